@@ -1,0 +1,85 @@
+"""Seeded synthetic inputs shaped like the attention workloads.
+
+This module draws random numbers and nothing else: it holds none of the
+attention arithmetic, so both the CUDA path and the fp64 oracle can be fed
+from it. Tensors are generated on the CPU with a seeded ``torch.Generator``
+in fp32 (Q, then K, then V) and rounded to the target dtype (bf16 rounding is
+round-to-nearest-even), so every consumer sees identical values.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    S: int
+    H: int
+    Hkv: int
+    D: int
+    dtype: str  # "bf16" or "f32"
+    causal: bool
+    window: int = -1  # -1: no sliding window
+    q_std: float = 1.0
+    k_std: float = 1.0
+    v_dist: str = "normal"  # "normal": N(0,1); "uniform": U(-1, 1)
+    seed: int = 1000
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / (self.D ** 0.5)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    def describe(self) -> str:
+        mask = "causal" if self.causal else "none"
+        if self.window > 0:
+            mask += f"+window{self.window}"
+        return (f"B{self.B} H{self.H} Hkv{self.Hkv} S{self.S} D{self.D} "
+                f"{self.dtype} {mask}")
+
+
+# The five workloads: a tiny fp32 case the oracle finishes instantly, a short
+# causal MHA case, a causal GQA case, a sliding-window GQA case and a
+# long-context multi-query stress case with large logits.
+WORKLOADS = {
+    "tiny_f32": Workload("tiny_f32", 1, 128, 2, 2, 64, "f32", False, seed=1000),
+    "mha_s1024_d64": Workload("mha_s1024_d64", 4, 1024, 16, 16, 64, "bf16", True, seed=1001),
+    "gqa_s4096_d128": Workload("gqa_s4096_d128", 2, 4096, 32, 8, 128, "bf16", True, seed=1002),
+    "swa_s16384_w4096": Workload("swa_s16384_w4096", 1, 16384, 32, 8, 128, "bf16", True,
+                                 window=4096, seed=1003),
+    "mqa_s32768_stress": Workload("mqa_s32768_stress", 1, 32768, 16, 1, 128, "bf16", True,
+                                  q_std=3.0, k_std=3.0, v_dist="uniform", seed=1004),
+}
+
+
+def make_qkv(B: int, S: int, H: int, Hkv: int, D: int, dtype: torch.dtype, seed: int,
+             q_std: float = 1.0, k_std: float = 1.0, v_dist: str = "normal"):
+    """Return CPU tensors q [B,S,H,D], k [B,S,Hkv,D], v [B,S,Hkv,D] in ``dtype``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((B, S, H, D), generator=g, dtype=torch.float32)
+    k = torch.randn((B, S, Hkv, D), generator=g, dtype=torch.float32)
+    if v_dist == "normal":
+        v = torch.randn((B, S, Hkv, D), generator=g, dtype=torch.float32)
+    elif v_dist == "uniform":
+        v = torch.rand((B, S, Hkv, D), generator=g, dtype=torch.float32) * 2.0 - 1.0
+    else:
+        raise ValueError(f"unknown v_dist {v_dist!r}")
+    if q_std != 1.0:
+        q = q * q_std
+    if k_std != 1.0:
+        k = k * k_std
+    return q.to(dtype), k.to(dtype), v.to(dtype)
+
+
+def workload_inputs(w: Workload, S: int | None = None, B: int | None = None):
+    """Inputs of a workload (optionally with a different S or B, same recipe)."""
+    return make_qkv(B or w.B, S or w.S, w.H, w.Hkv, w.D, w.torch_dtype, w.seed,
+                    q_std=w.q_std, k_std=w.k_std, v_dist=w.v_dist)

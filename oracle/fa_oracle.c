@@ -1,0 +1,197 @@
+/*
+ * fa_oracle.c -- plain fp64 CPU reference for the no-cache multi-head attention
+ * forward (the `mo.mha.no_cache` operator). TEST INFRASTRUCTURE ONLY: it is
+ * called by the tests, by the smoke check and by the benchmark's CPU-baseline
+ * leg, never by the product path. It shares no code with the CUDA library.
+ *
+ * What it computes, step by step as the MAX API page "FlashAttentionGPU"
+ * (method `execute`, Steps -1 to 4) describes the operator, for every batch b,
+ * query head h and query position i:
+ *
+ *   Step -1 (grouped attention): K and V may carry Hkv < H heads (BShD). The
+ *            page says only "G groups, h = H/G"; query head h reads KV head
+ *            h / G (consecutive query heads share one KV head, G = H / Hkv).
+ *            The alternative reading (KV head h % Hkv, a literal head-axis
+ *            concatenation) is selectable with head_map = 1.
+ *   Step 0  : the BSHD -> BHSD / BHDS transposes are index arithmetic here.
+ *   Step 1-3: s_j = scale * sum_d q[b,i,h,d] * k[b,j,hk,d]; keys the mask
+ *            hides get s_j = -inf (they are simply skipped below).
+ *   Step 4  : p_j = exp(s_j - m) / sum_j' exp(s_j' - m), m = max_j s_j;
+ *            out[b,i,h,:] = sum_j p_j v[b,j,hk,:]. This is the classic
+ *            attention of the Modular recipe "Custom Operations: Applications
+ *            in AI Models" (section "Limitations of classic attention"): bmm,
+ *            softmax, bmm, computed here one query row at a time.
+ *   LSE     : lse[b,h,i] = m + ln(sum_j exp(s_j - m)) (natural log, scale
+ *            included). The pages define no LSE output; this is its plain
+ *            definition.
+ *
+ * Mask (the page's `mask_str` / `local_window_size` parameters): key j is
+ * visible to query i iff (not causal or j <= i) and (window < 1 or
+ * i - j < window). window = -1 (or 0) means no window.
+ *
+ * Everything is fp64. Inputs are fp64 arrays (bf16 / fp32 values widen to
+ * fp64 exactly). The score row of one query is materialised (length S); the
+ * S x S matrix is not, which changes nothing in the arithmetic.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define FA_ORACLE_OK 0
+#define FA_ORACLE_BAD_ARG 1
+#define FA_ORACLE_NO_MEM 2
+
+typedef struct {
+  const double *q, *k, *v;
+  double *out, *lse;
+  long B, S, H, Hkv, D;
+  double scale;
+  int causal;
+  long window;
+  int head_map;
+  const long *rows;
+  long nrows;
+  long first, last; /* this worker's half-open range of (b, h, r) items */
+  int status;
+} fa_oracle_job;
+
+static int key_visible(long i, long j, int causal, long window) {
+  if (causal && j > i) return 0;
+  if (window > 0 && i - j >= window) return 0;
+  return 1;
+}
+
+static void *fa_oracle_worker(void *arg) {
+  fa_oracle_job *job = (fa_oracle_job *)arg;
+  const long S = job->S, H = job->H, Hkv = job->Hkv, D = job->D;
+  const long G = H / Hkv;
+  double *score = (double *)malloc(sizeof(double) * (size_t)S);
+  char *seen = (char *)malloc((size_t)S);
+  double *acc = (double *)malloc(sizeof(double) * (size_t)D);
+  if (!score || !seen || !acc) {
+    job->status = FA_ORACLE_NO_MEM;
+    free(score);
+    free(seen);
+    free(acc);
+    return NULL;
+  }
+  for (long item = job->first; item < job->last; ++item) {
+    /* item enumerates (b, h, r) with r fastest. */
+    const long r = item % job->nrows;
+    const long h = (item / job->nrows) % H;
+    const long b = item / (job->nrows * H);
+    const long i = job->rows ? job->rows[r] : r;
+    const long hk = job->head_map == 0 ? h / G : h % Hkv;
+
+    const double *qrow = job->q + ((b * job->nrows + r) * H + h) * D;
+
+    /* Steps 1-3: scaled scores of the visible keys, and their maximum. */
+    double m = -INFINITY;
+    for (long j = 0; j < S; ++j) {
+      seen[j] = (char)key_visible(i, j, job->causal, job->window);
+      if (!seen[j]) continue;
+      const double *krow = job->k + ((b * S + j) * Hkv + hk) * D;
+      double dot = 0.0;
+      for (long d = 0; d < D; ++d) dot += qrow[d] * krow[d];
+      score[j] = job->scale * dot;
+      if (score[j] > m) m = score[j];
+    }
+
+    /* Step 4: max-subtracted softmax, then the weighted sum of V rows. */
+    double denom = 0.0;
+    for (long d = 0; d < D; ++d) acc[d] = 0.0;
+    for (long j = 0; j < S; ++j) {
+      if (!seen[j]) continue;
+      const double e = exp(score[j] - m);
+      denom += e;
+      const double *vrow = job->v + ((b * S + j) * Hkv + hk) * D;
+      for (long d = 0; d < D; ++d) acc[d] += e * vrow[d];
+    }
+    double *orow = job->out + ((b * job->nrows + r) * H + h) * D;
+    for (long d = 0; d < D; ++d) orow[d] = acc[d] / denom; /* NaN if no key */
+    if (job->lse) job->lse[(b * H + h) * job->nrows + r] = m + log(denom);
+  }
+  free(score);
+  free(seen);
+  free(acc);
+  return NULL;
+}
+
+/*
+ * fa_oracle_forward
+ *   q    : [B, nrows, H, D] fp64 -- the query rows to evaluate. With rows ==
+ *          NULL, nrows must equal S and q is the whole BSHD query tensor.
+ *   k, v : [B, S, Hkv, D] fp64 (BSHD, or BShD when Hkv < H).
+ *   out  : [B, nrows, H, D] fp64, written.
+ *   lse  : [B, H, nrows] fp64 or NULL.
+ *   rows : NULL, or nrows query positions in [0, S) (the positions of q's rows).
+ *   causal, window: the mask (window <= 0 means no window).
+ *   head_map: 0 = grouped (h / G), 1 = tiled (h % Hkv).
+ *   nthreads: worker threads (>= 1).
+ * Returns 0 on success, 1 on a bad argument, 2 when memory runs out.
+ */
+int fa_oracle_forward(const double *q, const double *k, const double *v, double *out,
+                      double *lse, long B, long S, long H, long Hkv, long D, double scale,
+                      int causal, long window, int head_map, const long *rows, long nrows,
+                      int nthreads) {
+  if (!q || !k || !v || !out) return FA_ORACLE_BAD_ARG;
+  if (B < 1 || S < 1 || H < 1 || Hkv < 1 || D < 1 || H % Hkv != 0) return FA_ORACLE_BAD_ARG;
+  if (head_map != 0 && head_map != 1) return FA_ORACLE_BAD_ARG;
+  if (!rows) nrows = S;
+  if (nrows < 1) return FA_ORACLE_BAD_ARG;
+  if (rows)
+    for (long r = 0; r < nrows; ++r)
+      if (rows[r] < 0 || rows[r] >= S) return FA_ORACLE_BAD_ARG;
+  if (nthreads < 1) nthreads = 1;
+
+  const long items = B * H * nrows;
+  if (nthreads > items) nthreads = (int)items;
+  fa_oracle_job *jobs = (fa_oracle_job *)calloc((size_t)nthreads, sizeof(fa_oracle_job));
+  pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+  char *started = (char *)calloc((size_t)nthreads, 1);
+  if (!jobs || !tids || !started) {
+    free(jobs);
+    free(tids);
+    free(started);
+    return FA_ORACLE_NO_MEM;
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    fa_oracle_job *j = &jobs[t];
+    j->q = q;
+    j->k = k;
+    j->v = v;
+    j->out = out;
+    j->lse = lse;
+    j->B = B;
+    j->S = S;
+    j->H = H;
+    j->Hkv = Hkv;
+    j->D = D;
+    j->scale = scale;
+    j->causal = causal;
+    j->window = window;
+    j->head_map = head_map;
+    j->rows = rows;
+    j->nrows = nrows;
+    j->first = items * t / nthreads;
+    j->last = items * (t + 1) / nthreads;
+    j->status = FA_ORACLE_OK;
+  }
+  for (int t = 1; t < nthreads; ++t)
+    started[t] = pthread_create(&tids[t], NULL, fa_oracle_worker, &jobs[t]) == 0;
+  fa_oracle_worker(&jobs[0]);
+  int status = jobs[0].status;
+  for (int t = 1; t < nthreads; ++t) {
+    if (started[t]) {
+      pthread_join(tids[t], NULL);
+    } else {
+      fa_oracle_worker(&jobs[t]); /* thread creation failed: run inline */
+    }
+    if (jobs[t].status != FA_ORACLE_OK) status = jobs[t].status;
+  }
+  free(jobs);
+  free(tids);
+  free(started);
+  return status;
+}
