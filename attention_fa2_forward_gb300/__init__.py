@@ -1,1 +1,178 @@
-"""GB300-native fused multi-head attention forward (no KV cache)."""
+"""GB300-native fused multi-head attention forward without KV cache.
+
+Python binding of the C ABI in ``include/fa_mha.h`` (library
+``_build/libfa_mha.so``, built by :func:`build`). The binding only marshals
+arguments: it checks tensor placement/shape/dtype, allocates the outputs with
+torch and passes raw device pointers and the current CUDA stream to the
+library. Every step of the computation runs in the library's CUDA kernels;
+there is no fallback: if the library is missing or the GPU is not sm_103a the
+call raises.
+
+The operation is MAX's ``mo.mha.no_cache`` (API page "FlashAttentionGPU",
+method ``execute``): q in BSHD, k/v in BSHD or BShD (grouped-query attention,
+query head h reads KV head h // (H // Hkv)), output with q's shape and dtype,
+mask "none", "causal", or causal with a sliding window of W keys.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH, build  # noqa: F401  (re-exported)
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+DTYPE_BF16 = 0
+DTYPE_F32 = 1
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+
+# Every symbol the header declares (checked by the tests).
+EXPORTS = ("fa_mha_no_cache", "fa_device_status", "fa_set_wait_timeout_ns",
+           "fa_status_string", "fa_last_error_message", "fa_version", "fa_shutdown")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_string(status)}: {message}")
+        self.status = status
+
+
+def load_library(path: str | None = None):
+    """Open libfa_mha.so and declare the C signatures. Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"CUDA library {p} is not built; call attention_fa2_forward_gb300.build() "
+                "(nvcc, sm_103a) first")
+        lib = ctypes.CDLL(p)
+        vp, i = ctypes.c_void_p, ctypes.c_int
+        lib.fa_mha_no_cache.restype = i
+        lib.fa_mha_no_cache.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float,
+                                        i, i, i, vp]
+        lib.fa_device_status.restype = i
+        lib.fa_device_status.argtypes = [i, i]
+        lib.fa_set_wait_timeout_ns.restype = ctypes.c_ulonglong
+        lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_last_error_message.restype = ctypes.c_char_p
+        lib.fa_last_error_message.argtypes = []
+        lib.fa_version.restype = i
+        lib.fa_version.argtypes = []
+        lib.fa_shutdown.restype = None
+        lib.fa_shutdown.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().fa_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def _check(status: int):
+    if status != FA_OK:
+        msg = load_library().fa_last_error_message().decode()
+        raise FAError(status, msg)
+
+
+def _mask_code(mask) -> int:
+    if mask in (None, "none", MASK_NONE, False):
+        return MASK_NONE
+    if mask in ("causal", MASK_CAUSAL, True):
+        return MASK_CAUSAL
+    raise ValueError(f"unknown mask {mask!r} (use 'none' or 'causal')")
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return DTYPE_BF16
+    if dt == torch.float32:
+        return DTYPE_F32
+    raise TypeError(f"unsupported dtype {dt} (bf16 or fp32)")
+
+
+def mha_no_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
+                 mask="causal", window: int = -1, *, out: torch.Tensor | None = None,
+                 lse: torch.Tensor | None = None, return_lse: bool = False,
+                 stream: torch.cuda.Stream | None = None):
+    """Fused attention forward (``mo.mha.no_cache``) on the current CUDA device.
+
+    q: [B, S, H, D]; k, v: [B, S, Hkv, D]; all contiguous CUDA tensors of one
+    dtype (bf16 or fp32). ``scale`` defaults to 1/sqrt(D). ``mask`` is "none"
+    or "causal"; ``window`` > 0 adds a sliding window (causal only). Returns
+    out [B, S, H, D] (q's dtype), and lse [B, H, S] fp32 if ``return_lse``.
+    """
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D (BSHD)")
+    B, S, H, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != S or k.shape[3] != D:
+        raise ValueError(f"k/v shape {tuple(k.shape)}/{tuple(v.shape)} does not match q "
+                         f"{tuple(q.shape)} (expected [B, S, Hkv, D])")
+    Hkv = k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous (BSHD, D fastest)")
+        if t.dtype != q.dtype:
+            raise TypeError("q, k, v must share one dtype")
+        if t.device != q.device:
+            raise ValueError("q, k, v must be on one device")
+    dtype = _dtype_code(q.dtype)
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() \
+            or out.device != q.device:
+        raise ValueError("out must be a contiguous tensor with q's shape, dtype and device")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    elif lse is not None and (lse.shape != (B, H, S) or lse.dtype != torch.float32
+                              or not lse.is_contiguous() or lse.device != q.device):
+        raise ValueError("lse must be a contiguous fp32 [B, H, S] tensor on q's device")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = stream if stream is not None else torch.cuda.current_stream(q.device)
+        rc = lib.fa_mha_no_cache(
+            out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            q.data_ptr(), k.data_ptr(), v.data_ptr(),
+            B, S, H, Hkv, D, float(scale), _mask_code(mask), int(window), dtype,
+            st.cuda_stream)
+    _check(rc)
+    return (out, lse) if return_lse else out
+
+
+def device_status(device: int | None = None, clear: bool = True) -> int:
+    """Synchronise the device and return its sticky status (FA_OK or FA_ERR_TIMEOUT)."""
+    if device is None:
+        device = torch.cuda.current_device()
+    return int(load_library().fa_device_status(int(device), int(bool(clear))))
+
+
+def set_wait_timeout_ns(ns: int) -> int:
+    """Set the kernels' bounded-wait limit (0 restores the default); returns the old one."""
+    return int(load_library().fa_set_wait_timeout_ns(int(ns)))
+
+
+def version() -> int:
+    return int(load_library().fa_version())

@@ -1,0 +1,247 @@
+// fa_api.cu -- the C ABI declared in include/fa_mha.h: argument validation,
+// per-device state (status word), TMA tensor-map encoding and dispatch to the
+// bf16 tensor-core kernel or the fp32 CUDA-core kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa_mha.h"
+#include "fa_internal.h"
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
+
+std::mutex g_mutex;
+unsigned* g_status[kMaxDevices] = {};
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+thread_local char t_message[512] = "";
+
+fa_status_t fail(fa_status_t st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+fa_status_t fail(fa_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_message, sizeof(t_message), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+fa_status_t cuda_fail(cudaError_t err, const char* what) {
+  return fail(FA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+// Status word of the current device, created on first use.
+fa_status_t device_status_word(int dev, unsigned** out) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_status[dev] == nullptr) {
+    unsigned* p = nullptr;
+    cudaError_t err = cudaMalloc(&p, sizeof(unsigned));
+    if (err != cudaSuccess) return cuda_fail(err, "cudaMalloc(status word)");
+    err = cudaMemset(p, 0, sizeof(unsigned));
+    if (err != cudaSuccess) {
+      cudaFree(p);
+      return cuda_fail(err, "cudaMemset(status word)");
+    }
+    g_status[dev] = p;
+  }
+  *out = g_status[dev];
+  return FA_OK;
+}
+
+}  // namespace
+
+namespace fa {
+
+bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(heads) * D * 2,
+                                 static_cast<cuuint64_t>(S) * heads * D * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace fa
+
+extern "C" {
+
+fa_status_t fa_mha_no_cache(void* out, float* lse, const void* q, const void* k, const void* v,
+                            int B, int S, int H, int Hkv, int D, float scale, int mask_kind,
+                            int local_window_size, int dtype, void* stream) {
+  // ---- arguments (no CUDA call before these pass)
+  if (out == nullptr || q == nullptr || k == nullptr || v == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "null tensor pointer (out=%p q=%p k=%p v=%p)", out, q, k, v);
+  if (B < 1 || S < 1 || H < 1 || Hkv < 1)
+    return fail(FA_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d S=%d H=%d Hkv=%d)", B, S, H, Hkv);
+  if (H % Hkv != 0)
+    return fail(FA_ERR_INVALID_ARG, "H=%d is not a multiple of Hkv=%d", H, Hkv);
+  if (mask_kind != FA_MASK_NONE && mask_kind != FA_MASK_CAUSAL)
+    return fail(FA_ERR_INVALID_ARG, "unknown mask kind %d", mask_kind);
+  if (local_window_size == 0 || local_window_size < -1)
+    return fail(FA_ERR_INVALID_ARG, "local_window_size must be -1 or >= 1 (got %d)",
+                local_window_size);
+  if (local_window_size > 0 && mask_kind != FA_MASK_CAUSAL)
+    return fail(FA_ERR_INVALID_ARG, "a sliding window requires the causal mask");
+  if (!std::isfinite(scale))
+    return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+  if (scale < 0.f)
+    return fail(FA_ERR_UNSUPPORTED, "negative scale is not supported");
+  if (D != 64 && D != 128) return fail(FA_ERR_UNSUPPORTED, "head dim D=%d (built: 64, 128)", D);
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F32)
+    return fail(FA_ERR_UNSUPPORTED, "dtype %d", dtype);
+  const long long elems_q = static_cast<long long>(B) * S * H * D;
+  const long long row_bytes = static_cast<long long>(S) * H * D * 2;
+  if (elems_q >= (1ll << 40) || row_bytes >= (1ll << 39) ||
+      static_cast<long long>(B) * H * ((S + 255) / 256) > 0x7fffffffll)
+    return fail(FA_ERR_UNSUPPORTED, "problem too large (B=%d S=%d H=%d D=%d)", B, S, H, D);
+  const uintptr_t need = dtype == FA_DTYPE_BF16 ? 16 : 4;
+  if (!aligned(out, need) || !aligned(q, need) || !aligned(k, need) || !aligned(v, need) ||
+      (lse != nullptr && !aligned(lse, 4)))
+    return fail(FA_ERR_UNSUPPORTED, "tensors must be %u-byte aligned",
+                static_cast<unsigned>(need));
+
+  // ---- device
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(FA_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+  unsigned* status = nullptr;
+  fa_status_t st = device_status_word(dev, &status);
+  if (st != FA_OK) return st;
+
+  fa::FwdProblem p;
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.causal = mask_kind == FA_MASK_CAUSAL ? 1 : 0;
+  p.window = local_window_size > 0 ? local_window_size : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.lse = lse;
+  p.status = status;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == FA_DTYPE_BF16) {
+    err = fa::launch_fwd_bf16_tc(p, out, q, k, v, s);
+    if (err != cudaSuccess) return cuda_fail(err, "bf16 tensor-core kernel launch");
+  } else {
+    err = fa::launch_fwd_f32_simt(p, static_cast<float*>(out), static_cast<const float*>(q),
+                                  static_cast<const float*>(k), static_cast<const float*>(v), s);
+    if (err != cudaSuccess) return cuda_fail(err, "fp32 kernel launch");
+  }
+  return FA_OK;
+}
+
+fa_status_t fa_device_status(int device, int clear) {
+  if (device < 0 || device >= kMaxDevices)
+    return fail(FA_ERR_INVALID_ARG, "device index %d", device);
+  int prev = 0;
+  cudaError_t err = cudaGetDevice(&prev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if (prev != device && (err = cudaSetDevice(device)) != cudaSuccess)
+    return cuda_fail(err, "cudaSetDevice");
+  fa_status_t result = FA_OK;
+  err = cudaDeviceSynchronize();
+  if (err != cudaSuccess) {
+    result = cuda_fail(err, "cudaDeviceSynchronize");
+  } else {
+    unsigned* word = nullptr;
+    {
+      std::lock_guard<std::mutex> lock(g_mutex);
+      word = g_status[device];
+    }
+    if (word != nullptr) {
+      unsigned value = 0;
+      err = cudaMemcpy(&value, word, sizeof(value), cudaMemcpyDeviceToHost);
+      if (err != cudaSuccess) {
+        result = cuda_fail(err, "cudaMemcpy(status word)");
+      } else {
+        if (clear && value != 0 && (err = cudaMemset(word, 0, sizeof(unsigned))) != cudaSuccess)
+          result = cuda_fail(err, "cudaMemset(status word)");
+        else if (value & fa::kStatusWaitTimeout)
+          result = fail(FA_ERR_TIMEOUT, "a kernel on device %d gave up on a bounded wait", device);
+      }
+    }
+  }
+  if (prev != device) cudaSetDevice(prev);
+  return result;
+}
+
+unsigned long long fa_set_wait_timeout_ns(unsigned long long ns) {
+  return g_wait_limit_ns.exchange(ns == 0 ? kDefaultWaitLimitNs : ns);
+}
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+const char* fa_last_error_message(void) { return t_message; }
+
+int fa_version(void) { return kVersion; }
+
+void fa_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int prev = -1;
+  cudaGetDevice(&prev);
+  for (int d = 0; d < kMaxDevices; ++d) {
+    if (g_status[d] != nullptr) {
+      if (cudaSetDevice(d) == cudaSuccess) cudaFree(g_status[d]);
+      g_status[d] = nullptr;
+    }
+  }
+  if (prev >= 0) cudaSetDevice(prev);
+}
+
+}  // extern "C"

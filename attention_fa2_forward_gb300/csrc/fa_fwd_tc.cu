@@ -1,0 +1,556 @@
+// fa_fwd_tc.cu -- bf16 fused attention forward on the sm_103a tensor cores.
+//
+// The operation is `mo.mha.no_cache` (MAX API page "FlashAttentionGPU",
+// method `execute`, Steps -1 to 4): O = softmax(mask(scale * Q K^T)) V per
+// (batch, query head), Q/K/V/O in BSHD (K/V in BShD for grouped heads). The
+// algorithm is the FlashAttention-2 loop of the tiny_flash_attn.py page
+// (flash_attn_v2: Q blocks outer, KV blocks inner, running max m and running
+// sum l, unnormalised O rescaled by exp(m_old - m_new), one division by l at
+// the end), mapped onto Blackwell hardware:
+//
+//   * one CTA owns two 128-row Q tiles of one (b, h) and streams the K/V
+//     tiles both of them need through a shared-memory ring (TMA, 128-byte
+//     swizzle, straight from BSHD: the Step 0 / Step 4 transposes are the
+//     tensor maps' strides);
+//   * S = Q K^T and O += P V are tcgen05.mma (bf16 in, fp32 accumulate) with
+//     S, P and O resident in tensor memory: S_t at columns [128t, 128t+128),
+//     P_t (bf16 pairs) written over the first 64 of them, O_t at
+//     [256 + D t, 256 + D (t+1));
+//   * warp roles: warps 0-3 and 4-7 are the softmax warpgroups of Q tile 0 and
+//     1 (thread = query row = TMEM lane), warp 8 issues the MMAs, warp 9 the
+//     TMA loads. The MMA order S0 S1 | PV0 S0' PV1 S1' | ... lets one tile's
+//     softmax overlap the other tile's MMAs;
+//   * softmax in the log2 domain (exp2 of score * scale * log2 e minus the
+//     running max), with the rescale of O skipped while the running max grows
+//     by less than 2^8 (O and l keep the same stale max, so the final O / l is
+//     unchanged);
+//   * causal / sliding-window tiles that are entirely hidden are never loaded;
+//     only tiles that straddle the mask boundary evaluate the mask per element;
+//   * the epilogue writes O / l as bf16 through shared memory and a TMA store
+//     (BSHD), and the natural-log LSE per row.
+//
+// Every mbarrier wait is bounded by the problem's wait limit (global timer):
+// on time-out the CTA records kStatusWaitTimeout in the status word, stops
+// issuing work, waits (again bounded) for its own copies and MMAs in flight,
+// releases its tensor memory and returns.
+#include <cuda_bf16.h>
+
+#include <climits>
+#include <cmath>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;                          // query rows per Q tile (= TMEM lanes)
+constexpr int kBN = 128;                          // keys per K/V tile
+constexpr int kQTiles = 2;                        // Q tiles per CTA
+constexpr int kSoftmaxWarps = 4 * kQTiles;        // one warpgroup per Q tile
+constexpr int kMmaWarp = kSoftmaxWarps;           // warp 8
+constexpr int kLoadWarp = kSoftmaxWarps + 1;      // warp 9
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kBoxBytes = kBN * 128;              // [128 rows][64 bf16], 128B-swizzled
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;         // log2 units
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr unsigned long long kDrainExtraNs = 100000000ull;  // 100 ms
+
+template <int D>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;  // one [128][D] bf16 tile
+  static constexpr int kStages = D == 128 ? 4 : 6;       // K/V ring slots
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  // q_full[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] drain
+  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1 KB alignment
+  static constexpr uint32_t kColO = 256;                   // O_t at kColO + t * D
+};
+
+// Visibility bounds of query row i (keys lo..hi inclusive may be visible).
+struct RowBounds {
+  int lo, hi;
+};
+
+__device__ __forceinline__ RowBounds row_bounds(const FwdProblem& p, int i) {
+  RowBounds r;
+  r.lo = p.window > 0 ? i - p.window + 1 : INT_MIN;
+  r.hi = p.causal ? min(i, p.S - 1) : p.S - 1;
+  return r;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_o, const FwdProblem p,
+                          int num_qblocks) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+
+  const uint32_t sQ = base + C::kQOff;
+  const uint32_t sKV = base + C::kKVOff;
+  const uint32_t bars = base + C::kBarOff;
+  const uint32_t bar_q_full = bars;                              // + 8 t
+  const uint32_t bar_kv_full = bars + 8 * 2;                     // + 8 s
+  const uint32_t bar_kv_empty = bars + 8 * (2 + C::kStages);     // + 8 s
+  const uint32_t bar_s_full = bars + 8 * (2 + 2 * C::kStages);   // + 8 t
+  const uint32_t bar_p_full = bar_s_full + 16;                   // + 8 t
+  const uint32_t bar_o_full = bar_p_full + 16;                   // + 8 t
+  const uint32_t bar_drain = bar_o_full + 16;
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
+  // misc[0]: tensor-memory base address, misc[1]: abort flag
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work item: heaviest (last) query blocks first
+  const int per_qb = p.H * p.B;
+  const int qb = num_qblocks - 1 - static_cast<int>(blockIdx.x / per_qb);
+  const int rem = static_cast<int>(blockIdx.x % per_qb);
+  const int h = rem % p.H;
+  const int b = rem / p.H;
+  const int hk = h / (p.H / p.Hkv);
+
+  // KV tile range [lo_t, hi_t) of each Q tile; empty when the tile is past S.
+  int q0[kQTiles], lo[kQTiles], hi[kQTiles];
+#pragma unroll
+  for (int t = 0; t < kQTiles; ++t) {
+    q0[t] = qb * (kQTiles * kBM) + t * kBM;
+    if (q0[t] < p.S) {
+      const int kv_end = p.causal ? min(p.S, q0[t] + kBM) : p.S;
+      const int kv_begin = p.window > 0 ? max(0, q0[t] - p.window + 1) : 0;
+      lo[t] = kv_begin / kBN;
+      hi[t] = (kv_end + kBN - 1) / kBN;
+    } else {
+      lo[t] = hi[t] = 0;
+    }
+  }
+  const int jlo = lo[0];
+  const int jhi = max(hi[0], hi[1]);
+  const unsigned long long limit = p.wait_limit_ns;
+  const unsigned long long drain_limit = limit + kDrainExtraNs;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int t = 0; t < kQTiles; ++t) {
+      ptx::mbar_init(bar_q_full + 8 * t, 1);
+      ptx::mbar_init(bar_s_full + 8 * t, 1);
+      ptx::mbar_init(bar_p_full + 8 * t, 4);  // one arrival per softmax warp
+      ptx::mbar_init(bar_o_full + 8 * t, 1);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(bar_kv_full + 8 * s, 1);
+      ptx::mbar_init(bar_kv_empty + 8 * s, 1);
+    }
+    ptx::mbar_init(bar_drain, 1);
+    misc[1] = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    ptx::tma_prefetch_desc(&tm_q);
+    ptx::tma_prefetch_desc(&tm_k);
+    ptx::tma_prefetch_desc(&tm_v);
+    ptx::tma_prefetch_desc(&tm_o);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(base + C::kMiscOff, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  auto fail = [&]() {
+    misc[1] = 1;
+    atomicOr(p.status, kStatusWaitTimeout);
+  };
+  auto aborted = [&]() { return misc[1] != 0; };
+
+  if (warp == kLoadWarp) {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      const uint64_t pol_q = ptx::policy_evict_first();
+      const uint64_t pol_kv = ptx::policy_evict_last();
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t) {
+        if (lo[t] < hi[t]) {
+          ptx::mbar_arrive_expect_tx(bar_q_full + 8 * t, C::kTileBytes);
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            ptx::tma_load_4d(sQ + t * C::kTileBytes + bx * kBoxBytes, &tm_q, bar_q_full + 8 * t,
+                             bx * 64, h, q0[t], b, pol_q);
+        }
+      }
+      uint32_t armed = 0, armed_parity = 0;  // per slot: bit set once loaded / last parity
+      int idx = 0;
+      bool ok = true;
+      // Ring order: K_jlo, V_jlo, K_jlo+1, V_jlo+1, ...
+      for (int j = jlo; j < jhi && ok; ++j) {
+        for (int kind = 0; kind < 2; ++kind, ++idx) {
+          const int s = idx % C::kStages;
+          const uint32_t ph = static_cast<uint32_t>(idx / C::kStages) & 1u;
+          if (aborted() || !ptx::mbar_wait(bar_kv_empty + 8 * s, ph ^ 1u, limit)) {
+            fail();
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * s, C::kTileBytes);
+          const CUtensorMap* tm = kind == 0 ? &tm_k : &tm_v;
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            ptx::tma_load_4d(sKV + s * C::kTileBytes + bx * kBoxBytes, tm, bar_kv_full + 8 * s,
+                             bx * 64, hk, j * kBN, b, pol_kv);
+          armed |= 1u << s;
+          armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
+        }
+      }
+      // Never leave while a copy of ours may still be writing shared memory.
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t)
+        if (lo[t] < hi[t]) ptx::mbar_wait(bar_q_full + 8 * t, 0, drain_limit);
+      for (int s = 0; s < C::kStages; ++s)
+        if ((armed >> s) & 1u) ptx::mbar_wait(bar_kv_full + 8 * s, (armed_parity >> s) & 1u, drain_limit);
+    }
+  } else if (warp == kMmaWarp) {
+    // ===================================================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, D, false, true);
+      bool ok = true;
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t)
+        if (ok && lo[t] < hi[t] && !ptx::mbar_wait(bar_q_full + 8 * t, 0, limit)) {
+          fail();
+          ok = false;
+        }
+      auto in_tile = [&](int t, int j) { return j >= lo[t] && j < hi[t]; };
+      // Wait for ring entry idx; returns its slot or -1 on time-out.
+      auto wait_kv = [&](int idx) -> int {
+        const int s = idx % C::kStages;
+        const uint32_t ph = static_cast<uint32_t>(idx / C::kStages) & 1u;
+        if (aborted() || !ptx::mbar_wait(bar_kv_full + 8 * s, ph, limit)) {
+          fail();
+          return -1;
+        }
+        ptx::tc_fence_after();
+        return s;
+      };
+      // S_t = Q_t K^T: K-major A (Q) and B (K), K = D in steps of 16.
+      auto issue_s = [&](int t, int kslot) {
+        const uint32_t qa = sQ + t * C::kTileBytes;
+        const uint32_t kb = sKV + kslot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          const uint64_t da = ptx::smem_desc_sw128(qa + off, 16, 1024);
+          const uint64_t db = ptx::smem_desc_sw128(kb + off, 16, 1024);
+          ptx::mma_ss(tmem + t * kBN, da, db, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        ptx::tc_commit(bar_s_full + 8 * t);
+      };
+      // O_t (+)= P_t V: A = P_t from tensor memory, B = V (MN-major, N = D).
+      auto issue_pv = [&](int t, int vslot, bool accumulate) {
+        const uint32_t vb = sKV + vslot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint64_t dv = ptx::smem_desc_sw128(vb + kk * 2048, kBoxBytes, 1024);
+          ptx::mma_ts(tmem + C::kColO + t * D, tmem + t * kBN + kk * 8, dv, kIdescPV,
+                      (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+      uint32_t p_phase[kQTiles] = {0u, 0u};
+      auto wait_p = [&](int t) -> bool {
+        if (aborted() || !ptx::mbar_wait(bar_p_full + 8 * t, p_phase[t], limit)) {
+          fail();
+          return false;
+        }
+        p_phase[t] ^= 1u;
+        ptx::tc_fence_after();
+        return true;
+      };
+
+      if (ok) {
+        const int ks = wait_kv(0);
+        if (ks < 0) {
+          ok = false;
+        } else {
+#pragma unroll
+          for (int t = 0; t < kQTiles; ++t)
+            if (in_tile(t, jlo)) issue_s(t, ks);
+          ptx::tc_commit(bar_kv_empty + 8 * ks);
+        }
+      }
+      for (int j = jlo; ok && j < jhi; ++j) {
+        const int rel = j - jlo;
+        const int vs = wait_kv(2 * rel + 1);
+        if (vs < 0) break;
+        if (in_tile(0, j)) {
+          if (!wait_p(0)) break;
+          issue_pv(0, vs, j > lo[0]);
+          if (j == hi[0] - 1) ptx::tc_commit(bar_o_full);
+        }
+        const bool has_next = j + 1 < jhi;
+        int ks = -1;
+        if (has_next) {
+          ks = wait_kv(2 * rel + 2);
+          if (ks < 0) break;
+          if (in_tile(0, j + 1)) issue_s(0, ks);
+        }
+        if (in_tile(1, j)) {
+          if (!wait_p(1)) break;
+          issue_pv(1, vs, j > lo[1]);
+          if (j == hi[1] - 1) ptx::tc_commit(bar_o_full + 8);
+        }
+        ptx::tc_commit(bar_kv_empty + 8 * vs);
+        if (has_next) {
+          if (in_tile(1, j + 1)) issue_s(1, ks);
+          ptx::tc_commit(bar_kv_empty + 8 * ks);
+        }
+      }
+      // Every MMA must have finished before tensor memory is released.
+      ptx::tc_commit(bar_drain);
+      ptx::mbar_wait(bar_drain, 0, drain_limit);
+    }
+    __syncwarp();
+  } else {
+    // ===================================================== softmax warpgroups
+    const int t = warp >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    // This warpgroup's tile, selected without run-time array indexing.
+    const int tq0 = t == 0 ? q0[0] : q0[1];
+    const int tlo = t == 0 ? lo[0] : lo[1];
+    const int thi = t == 0 ? hi[0] : hi[1];
+    const int i = tq0 + row;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * kBN;
+    const uint32_t tO = tmem + lane_base + C::kColO + t * D;
+    const float c = p.scale_log2;
+    const RowBounds rb = row_bounds(p, i);
+
+    float m_use = -INFINITY;  // running max of score * scale * log2(e) (possibly stale)
+    float l_run = 0.f;        // running sum of 2^(x - m_use)
+    bool ok = true;
+    uint32_t s_phase = 0;
+    for (int j = tlo; j < thi; ++j) {
+      bool w = ptx::mbar_wait(bar_s_full + 8 * t, s_phase, limit);
+      s_phase ^= 1u;
+      w = __all_sync(0xffffffffu, w);
+      if (!w) {
+        fail();
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+
+      uint32_t r[kBN];
+#pragma unroll
+      for (int c0 = 0; c0 < kBN; c0 += 32) ptx::tmem_ld_32x32b_x32(tS + c0, r + c0);
+      ptx::tmem_wait_ld();
+      ptx::reg_fence<kBN>(r);
+
+      const int k0 = j * kBN;
+      bool full = k0 + kBN <= p.S;
+      if (p.causal) full = full && (k0 + kBN - 1 <= tq0);
+      if (p.window > 0) full = full && (tq0 + kBM - 1 - k0 < p.window);
+      const int vlo = rb.lo == INT_MIN ? INT_MIN : rb.lo - k0;
+      const int vhi = rb.hi - k0;
+
+      // Row maximum of the visible raw scores.
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      if (full) {
+#pragma unroll
+        for (int e = 0; e < kBN; e += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(r[e]));
+          mx1 = fmaxf(mx1, __uint_as_float(r[e + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(r[e + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(r[e + 3]));
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kBN; e += 4) {
+          mx0 = fmaxf(mx0, (e >= vlo && e <= vhi) ? __uint_as_float(r[e]) : -INFINITY);
+          mx1 = fmaxf(mx1, (e + 1 >= vlo && e + 1 <= vhi) ? __uint_as_float(r[e + 1]) : -INFINITY);
+          mx2 = fmaxf(mx2, (e + 2 >= vlo && e + 2 <= vhi) ? __uint_as_float(r[e + 2]) : -INFINITY);
+          mx3 = fmaxf(mx3, (e + 3 >= vlo && e + 3 <= vhi) ? __uint_as_float(r[e + 3]) : -INFINITY);
+        }
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float m_tile = mx == -INFINITY ? -INFINITY : mx * c;  // scale >= 0
+      const float m_new = fmaxf(m_use, m_tile);
+      const bool first = j == tlo;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (first) {
+        m_use = m_new;
+      } else if (m_new > m_use + kRescaleThreshold) {
+        alpha = ptx::ex2_approx(m_use - m_new);  // m_use may be -inf: alpha = 0
+        m_use = m_new;
+        rescale = true;
+      }
+      const float neg_base = m_use == -INFINITY ? 0.f : -m_use;
+
+      // P = 2^(x - m_use), row sum, and bf16 pairs written over S.
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      if (full) {
+#pragma unroll
+        for (int e = 0; e < kBN; e += 4) {
+          const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(r[e]), c, neg_base));
+          const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 1]), c, neg_base));
+          const float p2 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 2]), c, neg_base));
+          const float p3 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 3]), c, neg_base));
+          s0 += p0;
+          s1 += p1;
+          s2 += p2;
+          s3 += p3;
+          r[e / 2] = ptx::pack_bf16x2(p0, p1);
+          r[e / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kBN; e += 4) {
+          float p0 = ptx::ex2_approx(fmaf(__uint_as_float(r[e]), c, neg_base));
+          float p1 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 1]), c, neg_base));
+          float p2 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 2]), c, neg_base));
+          float p3 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 3]), c, neg_base));
+          p0 = (e >= vlo && e <= vhi) ? p0 : 0.f;
+          p1 = (e + 1 >= vlo && e + 1 <= vhi) ? p1 : 0.f;
+          p2 = (e + 2 >= vlo && e + 2 <= vhi) ? p2 : 0.f;
+          p3 = (e + 3 >= vlo && e + 3 <= vhi) ? p3 : 0.f;
+          s0 += p0;
+          s1 += p1;
+          s2 += p2;
+          s3 += p3;
+          r[e / 2] = ptx::pack_bf16x2(p0, p1);
+          r[e / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+        }
+      }
+      l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
+#pragma unroll
+      for (int c0 = 0; c0 < kBN / 2; c0 += 32) ptx::tmem_st_32x32b_x32(tS + c0, r + c0);
+
+      // Lazy correction of the O accumulator (previous PV has completed:
+      // the S MMA this iteration waited for was issued after it).
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          ptx::tmem_ld_32x32b_x32(tO + c0, o);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence<32>(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          ptx::tmem_st_32x32b_x32(tO + c0, o);
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_p_full + 8 * t);
+    }
+
+    // ---- epilogue: O / l -> bf16 -> shared (swizzled) -> TMA store; LSE.
+    const bool has_work = tlo < thi;
+    if (ok && has_work) {
+      bool w = ptx::mbar_wait(bar_o_full + 8 * t, 0, limit);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) {
+        fail();
+        ok = false;
+      }
+    }
+    const bool do_store = ok && has_work;
+    if (do_store) {
+      ptx::tc_fence_after();
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        ptx::tmem_ld_32x32b_x32(tO + c0, o);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<32>(o);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 pk;
+          pk.x = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l,
+                                  __uint_as_float(o[8 * u + 1]) * inv_l);
+          pk.y = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l,
+                                  __uint_as_float(o[8 * u + 3]) * inv_l);
+          pk.z = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l,
+                                  __uint_as_float(o[8 * u + 5]) * inv_l);
+          pk.w = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l,
+                                  __uint_as_float(o[8 * u + 7]) * inv_l);
+          const int chunk = ((c0 & 63) >> 3) + u;  // 16-byte chunk within the 128-byte row
+          const int box = c0 >> 6;
+          const int phys = chunk ^ (row & 7);       // 128-byte swizzle
+          *reinterpret_cast<uint4*>(stage + box * kBoxBytes + row * 128 + phys * 16) = pk;
+        }
+      }
+      ptx::fence_proxy_async_smem();
+    }
+    ptx::named_bar_sync(1 + t, 128);
+    if (do_store && quad == 0 && lane == 0) {
+#pragma unroll
+      for (int bx = 0; bx < C::kBoxes; ++bx)
+        ptx::tma_store_4d(&tm_o, sQ + t * C::kTileBytes + bx * kBoxBytes, bx * 64, h, tq0, b);
+      ptx::tma_store_commit();
+      ptx::tma_store_wait_read();
+    }
+    if (do_store && p.lse != nullptr && i < p.S) {
+      const float m_fin = m_use == -INFINITY ? 0.f : m_use;
+      p.lse[(static_cast<size_t>(b) * p.H + h) * p.S + i] = (m_fin + __log2f(l_run)) * kLn2;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* k, const void* v,
+                     cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, to;
+  if (!encode_bshd_tensor_map(&tq, q, p.B, p.S, p.H, D) ||
+      !encode_bshd_tensor_map(&tk, k, p.B, p.S, p.Hkv, D) ||
+      !encode_bshd_tensor_map(&tv, v, p.B, p.S, p.Hkv, D) ||
+      !encode_bshd_tensor_map(&to, out, p.B, p.S, p.H, D))
+    return cudaErrorInvalidValue;
+  const int nqb = (p.S + kQTiles * kBM - 1) / (kQTiles * kBM);
+  const long long grid = static_cast<long long>(nqb) * p.H * p.B;
+  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+  cudaError_t err = cudaFuncSetAttribute(fa_fwd_bf16_tc_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<D>::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  fa_fwd_bf16_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(
+      tq, tk, tv, to, p, nqb);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, const void* k,
+                               const void* v, cudaStream_t stream) {
+  if (p.D == 64) return launch_d<64>(p, out, q, k, v, stream);
+  if (p.D == 128) return launch_d<128>(p, out, q, k, v, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

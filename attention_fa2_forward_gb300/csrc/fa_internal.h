@@ -1,0 +1,40 @@
+// fa_internal.h -- declarations shared by the host C-ABI and the kernels'
+// launchers (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fa {
+
+// Bits of the per-device status word the kernels may set.
+constexpr unsigned kStatusWaitTimeout = 1u;
+
+// Problem description handed to both kernels by value.
+struct FwdProblem {
+  int B, S, H, Hkv, D;
+  int causal;            // 1: key j visible to query i only if j <= i
+  int window;            // > 0: also require i - j < window
+  float scale;           // multiplies q.k
+  float scale_log2;      // scale * log2(e)
+  float* lse;            // [B, H, S] fp32 or nullptr
+  unsigned* status;      // device status word (sticky error bits)
+  unsigned long long wait_limit_ns;
+};
+
+// Tensor-core (tcgen05) bf16 forward. q/k/v/out are device pointers to
+// 16-byte-aligned dense BSHD / BShD bf16 tensors. Returns a cudaError_t.
+cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, const void* k,
+                               const void* v, cudaStream_t stream);
+
+// CUDA-core fp32 forward for fp32 tensors.
+cudaError_t launch_fwd_f32_simt(const FwdProblem& p, float* out, const float* q, const float* k,
+                                const float* v, cudaStream_t stream);
+
+// Encodes a 4-D BSHD tensor map (dims D, heads, S, B) for bf16 data with a
+// {64, 1, 128, 1} box and 128-byte swizzle. Returns false on failure.
+bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D);
+
+}  // namespace fa

@@ -1,0 +1,426 @@
+"""Benchmark of the fused attention forward (no KV cache) on GB300.
+
+One step = one forward pass of the whole hot path (one kernel launch) over
+one batch of the workload's synthetic inputs, resident in HBM. L2 is flushed
+(a 256 MiB buffer is rewritten) before every timed step and each step's
+kernel is timed with CUDA events on the launching stream.
+
+Prints ONE JSON line (rank 0). Metric: attention forward TFLOP/s counting
+only unmasked (query, key) pairs, FLOPs = 4 * B * H * D * pairs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+--impl reference times the fp64 CPU oracle on the host cores over a bounded
+sample of the same workload (the reference arm of this benchmark).
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload (no data-path collective; the workload's (batch, head) units are
+independent), timings are max-reduced over ranks, scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "gqa_s4096_d128"
+METRIC = "attention fwd TFLOP/s (unmasked FLOPs) and % of GB300 BF16 tensor peak"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_NAME = "fa_fwd_bf16_tc_kernel"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- FLOP accounting
+def visible_pairs(S: int, causal: bool, window: int) -> int:
+    """Number of (query, key) pairs the mask leaves visible in one (b, h)."""
+    if not causal:
+        return S * S
+    if window is None or window <= 0 or window >= S:
+        return S * (S + 1) // 2
+    W = window
+    return W * (W + 1) // 2 + (S - W) * W
+
+
+def visible_keys_of_row(i: int, S: int, causal: bool, window: int) -> int:
+    hi = i if causal else S - 1
+    lo = max(0, i - window + 1) if (causal and window and window > 0) else 0
+    return hi - lo + 1
+
+
+def workload_flops(w) -> float:
+    return 4.0 * w.B * w.H * w.D * visible_pairs(w.S, w.causal, w.window)
+
+
+def algorithmic_bytes(w) -> int:
+    """Minimum HBM traffic of one launch: read Q, K, V once, write O and LSE."""
+    e = 2 if w.dtype == "bf16" else 4
+    return (2 * w.B * w.S * w.H * w.D * e + 2 * w.B * w.S * w.Hkv * w.D * e
+            + 4 * w.B * w.H * w.S)
+
+
+# ----------------------------------------------------------------- peaks / traffic
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest() -> str:
+    csrc = os.path.join(ROOT, "attention_fa2_forward_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("fa_fwd_tc") or name.endswith((".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (matching digest); else None."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)\s*\(kernel source digest ([0-9a-f]+)\)",
+                  text)
+    if not m or m.group(2) != kernel_source_digest():
+        return None
+    return int(m.group(1))
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (ctypes) while the
+    timed region runs. Reads settings only."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x10: "sync_boost"}
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.index, self.period = index, period_s
+        self.samples, self.reasons = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.ok = False
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.handle)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            self.ok = False
+
+    def _sample(self):
+        mhz = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
+            self.samples.append(mhz.value)
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        if fn(self.handle, ctypes.byref(rs)) == 0:
+            for bit, name in self.REASONS.items():
+                if rs.value & bit:
+                    self.reasons.add(name)
+
+    def _run(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self.ok and self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            if not self.samples:
+                self._sample()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29511")
+        dist.init_process_group(backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(value: float, dist) -> float:
+    if dist is None:
+        return value
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- oracle sample
+def oracle_sample_rows(w, target_flops: float):
+    """Evenly spread query rows whose oracle work is about target_flops."""
+    total = workload_flops(w)
+    frac = min(1.0, target_flops / total)
+    n = max(2, int(round(w.S * frac)))
+    if n >= w.S:
+        return list(range(w.S))
+    step = w.S / n
+    return sorted({min(w.S - 1, int(i * step + step / 2)) for i in range(n)})
+
+
+def sampled_flops(w, rows) -> float:
+    keys = sum(visible_keys_of_row(i, w.S, w.causal, w.window) for i in rows)
+    return 4.0 * w.B * w.H * w.D * keys
+
+
+def run_oracle_sample(w, q, k, v, rows, nthreads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.mha_forward(q[:, rows], k, v, w.scale, w.causal, w.window, rows=rows,
+                       nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+# ----------------------------------------------------------------- arms
+def bench_reference(args, w, world, rank):
+    """The fp64 oracle on the host cores: each step evaluates a bounded,
+    evenly spread sample of the workload's query rows (all batches, heads)."""
+    if rank != 0:
+        return None
+    import oracle
+    from attention_fa2_forward_gb300.inputs import workload_inputs
+    oracle.build()
+    q, k, v = workload_inputs(w)
+    nthreads = oracle.default_threads()
+    # Size the per-step sample from a short calibration run.
+    probe_rows = oracle_sample_rows(w, 2e9)
+    t = run_oracle_sample(w, q, k, v, probe_rows, nthreads)
+    rate = sampled_flops(w, probe_rows) / max(t, 1e-6)
+    per_step_s = max(0.2, min(8.0, 120.0 / max(1, args.steps + args.warmup)))
+    rows = oracle_sample_rows(w, rate * per_step_s)
+    for _ in range(args.warmup):
+        run_oracle_sample(w, q, k, v, rows, nthreads)
+    times = [run_oracle_sample(w, q, k, v, rows, nthreads) for _ in range(args.steps)]
+    fl = sampled_flops(w, rows)
+    total_s = sum(times)
+    value = fl * args.steps / total_s / 1e12
+    sample = (f"{len(rows)} of {w.S} query rows (evenly spread), all {w.B} batches x {w.H} heads, "
+              f"{fl / 1e9:.2f} GFLOP per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.describe(), "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def bench_ours(args, w, world, rank, local, dist):
+    import torch
+
+    import attention_fa2_forward_gb300 as fa
+    from attention_fa2_forward_gb300.inputs import workload_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    q_h, k_h, v_h = workload_inputs(w)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    mask = "causal" if w.causal else "none"
+
+    def step():
+        fa.mha_no_cache(q, k, v, w.scale, mask, w.window, out=out, lse=lse)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if fa.device_status() != fa.FA_OK:
+        raise RuntimeError("kernel reported a timed-out wait during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        starts[s].record(stream)
+        step()
+        ends[s].record(stream)
+    torch.cuda.synchronize()
+    wall_s = time.perf_counter() - t_wall
+    clocks.stop()
+    barrier(dist)
+    kernel_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    local_ms = sum(kernel_ms)
+    total_ms = max_over_ranks(local_ms, dist)
+    if fa.device_status() != fa.FA_OK:
+        raise RuntimeError("kernel reported a timed-out wait in the timed region")
+
+    # ---- end to end through the public API, host buffers, copies in the timed region
+    e2e = None
+    if not args.no_e2e:
+        qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+        outp = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        e2e_steps = max(1, min(args.steps, 20))
+
+        def e2e_step():
+            q.copy_(qp, non_blocking=True)
+            k.copy_(kp, non_blocking=True)
+            v.copy_(vp, non_blocking=True)
+            fa.mha_no_cache(q, k, v, w.scale, mask, w.window, out=out)
+            outp.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(dist)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist) / e2e_steps
+        h2d = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
+        d2h = outp.numel() * outp.element_size()
+        e2e = {"value": world * workload_flops(w) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    # ---- CPU baseline: the oracle on a bounded sample, rank 0 at N=1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        nthreads = oracle.default_threads()
+        rows = oracle_sample_rows(w, 2e9)
+        t = run_oracle_sample(w, q_h, k_h, v_h, rows, nthreads)
+        rate = sampled_flops(w, rows) / max(t, 1e-6)
+        rows = oracle_sample_rows(w, rate * args.cpu_seconds)
+        t = run_oracle_sample(w, q_h, k_h, v_h, rows, nthreads)
+        fl = sampled_flops(w, rows)
+        cpu = {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+               "sample": f"{len(rows)} of {w.S} query rows (evenly spread), all {w.B} batches "
+                         f"x {w.H} heads: {fl / 1e9:.1f} GFLOP in {t:.1f} s"}
+
+    flops = workload_flops(w)
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (local_ms / args.steps * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                "peak_source": f"{peak_src} (bf16 burst, MEASURED_PEAKS.json)"
+                if peak_src == "measured" else "fallback",
+                "algorithmic_bytes": algorithmic_bytes(w),
+                "hbm_gbs": algorithmic_bytes(w) / (local_ms / args.steps * 1e-3) / 1e9}
+    return {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.describe(), "B": w.B, "S": w.S, "H": w.H,
+                   "Hkv": w.Hkv, "D": w.D, "mask": mask, "window": w.window,
+                   "flops_per_step": flops, "l2": "flushed (256 MiB write) before every step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_peak": 100.0 * value / (peak * world),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": clocks.summary(), "gpu_launches": args.steps,
+        "wall_s_timed_region": wall_s,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from attention_fa2_forward_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        res = bench_reference(args, w, world, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+    dist = init_dist(world, "nccl")
+    res = bench_ours(args, w, world, rank, local, dist)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,121 @@
+/*
+ * fa_mha.h -- C ABI of the GB300 (sm_103a) fused multi-head attention forward
+ * without KV cache.
+ *
+ * The operation is the `mo.mha.no_cache` operator documented on the MAX API
+ * page "FlashAttentionGPU" (method `execute`, Steps -1 to 4, and its
+ * Parameters / Args lists):
+ *
+ *   out[b,i,h,:] = sum_j softmax_j( mask( scale * q[b,i,h,:] . k[b,j,hk,:] ) ) v[b,j,hk,:]
+ *
+ * with q, k, v and out in BSHD layout (the transposes of Step 0 and Step 4 are
+ * folded into the kernel's addressing), grouped-query attention when k/v
+ * carry Hkv < H heads (BShD; query head h reads KV head hk = h / (H / Hkv),
+ * i.e. consecutive query heads share a KV head), and a mask that is none,
+ * causal (key j visible to query i iff j <= i), or causal with a sliding
+ * window of W keys (visible iff j <= i and i - j < W). The S x S score matrix
+ * is never materialised: the bf16 path is a FlashAttention-2 style kernel
+ * (online softmax over KV tiles, one final division by the running sum) on
+ * the sm_103a tensor cores.
+ *
+ * Every buffer is owned by the caller. All entry points are plain C; device
+ * pointers are CUDA device addresses on the current device, `stream` is a
+ * cudaStream_t passed as void* (NULL = legacy default stream).
+ */
+#ifndef FA_MHA_H_
+#define FA_MHA_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Mask kinds (the page's `mask_str`, chosen at run time here). */
+#define FA_MASK_NONE 0
+#define FA_MASK_CAUSAL 1
+
+/* Element types of q, k, v and out (all four share one type). */
+#define FA_DTYPE_BF16 0 /* tensor-core path, fp32 accumulation, bf16 output */
+#define FA_DTYPE_F32 1  /* CUDA-core fp32 path (exact fp32 FMA arithmetic) */
+
+/* Status codes returned by every entry point. */
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* a null pointer, a bad size, a bad mask/window */
+  FA_ERR_UNSUPPORTED = 2, /* valid but not built: D, dtype, GPU arch, alignment */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  FA_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait (see fa_device_status) */
+} fa_status_t;
+
+/*
+ * fa_mha_no_cache -- the fused attention forward (FlashAttentionGPU.execute).
+ *
+ *   out   : device, [B, S, H, D], same dtype as q (the page: "same shape as q").
+ *   lse   : device, [B, H, S] fp32, or NULL. Per query row the natural-log
+ *           log-sum-exp of the scaled, masked scores (not on the pages; the
+ *           statistic a split-KV combine consumes).
+ *   q     : device, [B, S, H, D] (BSHD).
+ *   k, v  : device, [B, S, Hkv, D] (BSHD when Hkv == H, BShD otherwise).
+ *   B, S, H, Hkv, D : sizes; B, S, H, Hkv >= 1, H % Hkv == 0, D in {64, 128}.
+ *   scale : multiplies q.k before masking and softmax (the page's `scale`);
+ *           finite and >= 0.
+ *   mask_kind : FA_MASK_NONE or FA_MASK_CAUSAL.
+ *   local_window_size : -1 for no window, else W >= 1 (only with
+ *           FA_MASK_CAUSAL): query i sees keys i-W+1 .. i.
+ *   dtype : FA_DTYPE_BF16 or FA_DTYPE_F32.
+ *   stream: cudaStream_t (as void*) the work is enqueued on.
+ *
+ * Layout: dense and contiguous, D fastest. bf16 buffers must be 16-byte
+ * aligned (the kernel reads them with TMA). Sizes must keep every tensor
+ * below 2^31 elements per dimension product used in indexing (checked).
+ *
+ * Behaviour: asynchronous on `stream`; returns after validation and launch.
+ * Argument errors return FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED before any
+ * CUDA call. A kernel that exceeds its bounded-wait limit abandons its tile,
+ * sets a sticky per-device status word and leaves the outputs of that tile
+ * undefined; read it with fa_device_status(). The first call on a device
+ * allocates that 4-byte status word (cudaMalloc) and sets kernel attributes;
+ * fa_shutdown() frees it. Thread-safe.
+ */
+fa_status_t fa_mha_no_cache(void *out, float *lse, const void *q, const void *k, const void *v,
+                            int B, int S, int H, int Hkv, int D, float scale, int mask_kind,
+                            int local_window_size, int dtype, void *stream);
+
+/*
+ * fa_device_status -- synchronises `device` (cudaDeviceSynchronize) and reads
+ * its sticky status word: FA_OK, or FA_ERR_TIMEOUT if any kernel since the
+ * last clear abandoned a bounded wait. With clear != 0 the word is reset.
+ * Returns FA_ERR_CUDA if the synchronisation itself reports an error.
+ */
+fa_status_t fa_device_status(int device, int clear);
+
+/*
+ * fa_set_wait_timeout_ns -- limit, in nanoseconds of GPU global timer, of
+ * every spin-wait inside the kernels (default 2e9). A value of 0 restores the
+ * default. Affects launches made after the call. Returns the previous limit.
+ */
+unsigned long long fa_set_wait_timeout_ns(unsigned long long ns);
+
+/* fa_status_string -- a static, human-readable name for a status code. */
+const char *fa_status_string(int status);
+
+/*
+ * fa_last_error_message -- detail of the last non-OK status returned on the
+ * calling thread (which argument was rejected, which CUDA call failed).
+ * The string is owned by the library and valid until the next call.
+ */
+const char *fa_last_error_message(void);
+
+/* fa_version -- library version as major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+/*
+ * fa_shutdown -- frees the per-device status words. Call only when no work
+ * issued by this library is pending; later calls re-create what they need.
+ */
+void fa_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_MHA_H_ */

@@ -1,0 +1,87 @@
+"""The C-ABI library loads without a GPU, exports every symbol the header
+declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_fa2_forward_gb300 as fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa_mha.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa.build()
+    return fa.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared_functions() == sorted(fa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings(lib):
+    assert fa.version() == 100
+    assert lib.fa_status_string(0) == b"FA_OK"
+    assert lib.fa_status_string(4) == b"FA_ERR_TIMEOUT"
+    assert lib.fa_status_string(99) == b"FA_ERR_UNKNOWN"
+
+
+def test_wait_timeout_setting_roundtrip(lib):
+    old = fa.set_wait_timeout_ns(12345)
+    assert fa.set_wait_timeout_ns(0) == 12345
+    assert fa.set_wait_timeout_ns(old) == 2_000_000_000
+
+
+P = 0x10000  # a non-null, 16-byte aligned fake address: never dereferenced
+
+
+def _call(lib, out=P, lse=None, q=P, k=P, v=P, B=1, S=8, H=2, Hkv=2, D=64, scale=0.125,
+          mask=1, window=-1, dtype=0):
+    return lib.fa_mha_no_cache(out, lse, q, k, v, B, S, H, Hkv, D, scale, mask, window, dtype,
+                               None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(out=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(S=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=3, Hkv=2), fa.FA_ERR_INVALID_ARG),
+    (dict(Hkv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(mask=2), fa.FA_ERR_INVALID_ARG),
+    (dict(window=0), fa.FA_ERR_INVALID_ARG),
+    (dict(window=-2), fa.FA_ERR_INVALID_ARG),
+    (dict(mask=0, window=4), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=7), fa.FA_ERR_UNSUPPORTED),
+    (dict(q=P + 8), fa.FA_ERR_UNSUPPORTED),  # bf16 tensors need 16-byte alignment
+    (dict(S=1 << 30, H=1 << 10), fa.FA_ERR_UNSUPPORTED),
+])
+def test_argument_validation_happens_before_cuda(lib, kw, code):
+    assert _call(lib, **kw) == code
+    assert lib.fa_last_error_message()  # a reason is recorded
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 4, 2, 64)
+    with pytest.raises(ValueError):
+        fa.mha_no_cache(q, q, q)

@@ -1,0 +1,172 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle on
+the same seeded inputs.
+
+Tolerances: bf16 inputs with fp32 accumulation must be within max-abs 2e-2
+and mean-abs 2e-3 of the fp64 result; the fp32 path within max-abs 1e-4.
+The log-sum-exp rows are compared with max-abs 2e-3 (bf16 path: scores are
+exact products of bf16 values accumulated in fp32; exp2/log2 are the
+hardware approximations) and 1e-4 (fp32 path).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import attention_fa2_forward_gb300 as fa
+from attention_fa2_forward_gb300.inputs import WORKLOADS, make_qkv, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX, BF16_MEAN, BF16_LSE = 2e-2, 2e-3, 2e-3
+F32_MAX, F32_LSE = 1e-4, 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    fa.build()
+    fa.load_library()
+    yield
+    assert fa.device_status() == fa.FA_OK
+
+
+def _run_gpu(q, k, v, scale, causal, window, poison=True):
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    out = torch.empty_like(qd)
+    B, S, H, _ = q.shape
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    if poison:
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+    fa.mha_no_cache(qd, kd, vd, scale, "causal" if causal else "none", window, out=out, lse=lse)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+def _compare(out, lse, ref_out, ref_lse, dtype, label):
+    assert np.isfinite(out).all(), f"{label}: non-finite output"
+    assert np.isfinite(lse).all(), f"{label}: non-finite lse"
+    err = np.abs(out - ref_out)
+    lerr = np.abs(lse - ref_lse)
+    if dtype == torch.bfloat16:
+        assert err.max() <= BF16_MAX, f"{label}: max-abs {err.max():.3e}"
+        assert err.mean() <= BF16_MEAN, f"{label}: mean-abs {err.mean():.3e}"
+        assert lerr.max() <= BF16_LSE, f"{label}: lse max-abs {lerr.max():.3e}"
+    else:
+        assert err.max() <= F32_MAX, f"{label}: max-abs {err.max():.3e}"
+        assert lerr.max() <= F32_LSE, f"{label}: lse max-abs {lerr.max():.3e}"
+    return float(err.max()), float(err.mean())
+
+
+def _full_case(oracle_mod, B, S, H, Hkv, D, dtype, causal, window, seed, scale=None,
+               q_std=1.0, k_std=1.0, v_dist="normal"):
+    q, k, v = make_qkv(B, S, H, Hkv, D, dtype, seed, q_std=q_std, k_std=k_std, v_dist=v_dist)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out, lse = _run_gpu(q, k, v, scale, causal, window)
+    ref_out, ref_lse = oracle_mod.mha_forward(q, k, v, scale, causal, window)
+    label = f"B{B} S{S} H{H}/{Hkv} D{D} {dtype} causal={causal} W={window}"
+    return _compare(out, lse, ref_out, ref_lse, dtype, label)
+
+
+# --- the tiny fp32 workload and the short causal MHA workload, whole ---------------
+
+def test_tiny_fp32_workload(oracle_mod):
+    w = WORKLOADS["tiny_f32"]
+    q, k, v = workload_inputs(w)
+    out, lse = _run_gpu(q, k, v, w.scale, w.causal, w.window)
+    ref_out, ref_lse = oracle_mod.mha_forward(q, k, v, w.scale, w.causal, w.window)
+    _compare(out, lse, ref_out, ref_lse, torch.float32, w.name)
+
+
+def test_mha_s1024_d64_workload_whole(oracle_mod):
+    w = WORKLOADS["mha_s1024_d64"]
+    q, k, v = workload_inputs(w)
+    out, lse = _run_gpu(q, k, v, w.scale, w.causal, w.window)
+    ref_out, ref_lse = oracle_mod.mha_forward(q, k, v, w.scale, w.causal, w.window)
+    _compare(out, lse, ref_out, ref_lse, torch.bfloat16, w.name)
+
+
+# --- the long workloads at full size, on sampled query rows -------------------------
+
+def _sample_rows(S, seed, n_random=40):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 2, 63, 64, 127, 128, 129, 255, 256, 257, 511, 4095, 4096, 4097,
+             S // 2, S - 257, S - 129, S - 128, S - 2, S - 1]
+    rows = {r for r in fixed if 0 <= r < S}
+    rows.update(int(r) for r in rng.integers(0, S, n_random))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", ["gqa_s4096_d128", "swa_s16384_w4096", "mqa_s32768_stress"])
+def test_full_size_workload_sampled_rows(oracle_mod, name):
+    w = WORKLOADS[name]
+    q, k, v = workload_inputs(w)
+    out, lse = _run_gpu(q, k, v, w.scale, w.causal, w.window)
+    rows = _sample_rows(w.S, w.seed)
+    ref_out, ref_lse = oracle_mod.mha_forward(q[:, rows], k, v, w.scale, w.causal, w.window,
+                                              rows=rows)
+    _compare(out[:, rows], lse[:, :, rows], ref_out, ref_lse, torch.bfloat16, name)
+    # Every element was written (the buffers were NaN-poisoned).
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+# --- edge shapes -------------------------------------------------------------------
+
+EDGE_SHAPES = [
+    # S, H, Hkv, D, causal, window
+    (1, 2, 2, 64, False, -1),
+    (1, 2, 1, 128, True, -1),
+    (2, 2, 2, 64, True, -1),
+    (127, 4, 2, 64, False, -1),
+    (128, 2, 2, 128, True, -1),
+    (129, 4, 4, 128, True, -1),
+    (129, 2, 1, 64, False, -1),
+    (255, 2, 2, 64, True, 1),
+    (256, 4, 2, 128, True, 2),
+    (257, 4, 1, 64, True, 127),
+    (300, 2, 2, 128, True, 128),
+    (513, 4, 2, 64, True, 129),
+    (513, 2, 2, 128, False, -1),
+    (640, 4, 4, 128, True, 640),
+    (700, 2, 1, 128, True, 300),
+    (1000, 2, 2, 64, True, -1),
+]
+
+
+@pytest.mark.parametrize("S,H,Hkv,D,causal,window", EDGE_SHAPES)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_edge_shapes(oracle_mod, S, H, Hkv, D, causal, window, dtype):
+    _full_case(oracle_mod, 2, S, H, Hkv, D, dtype, causal, window, seed=7 + S)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_scale_zero_averages_visible_values(oracle_mod, dtype):
+    _full_case(oracle_mod, 1, 300, 2, 1, 128, dtype, True, 100, seed=11, scale=0.0)
+
+
+def test_large_logits_rescaling(oracle_mod):
+    # Logits with standard deviation ~9: stresses the online-softmax rescale.
+    _full_case(oracle_mod, 1, 1100, 4, 1, 128, torch.bfloat16, True, -1, seed=12,
+               q_std=3.0, k_std=3.0, v_dist="uniform")
+    _full_case(oracle_mod, 1, 600, 2, 2, 64, torch.bfloat16, False, -1, seed=13,
+               q_std=4.0, k_std=4.0, v_dist="uniform")
+
+
+def test_batches_are_independent(oracle_mod):
+    _full_case(oracle_mod, 3, 384, 4, 2, 128, torch.bfloat16, True, -1, seed=14)
+
+
+def test_deterministic_and_stream_aware(oracle_mod):
+    q, k, v = make_qkv(2, 1000, 8, 2, 128, torch.bfloat16, 15)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    a = fa.mha_no_cache(qd, kd, vd, 0.09, "causal")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        b = fa.mha_no_cache(qd, kd, vd, 0.09, "causal")
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
