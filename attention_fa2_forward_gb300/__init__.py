@@ -35,8 +35,9 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 
 # Every symbol the header declares (checked by the tests).
-EXPORTS = ("fa_mha_no_cache", "fa_device_status", "fa_set_wait_timeout_ns",
-           "fa_status_string", "fa_last_error_message", "fa_version", "fa_shutdown")
+EXPORTS = ("fa_mha_no_cache", "fa_device_status",
+           "fa_set_wait_timeout_ns", "fa_set_stall_probe", "fa_status_string",
+           "fa_last_error_message", "fa_version", "fa_shutdown")
 
 _lib = None
 _lock = threading.Lock()
@@ -68,6 +69,8 @@ def load_library(path: str | None = None):
         lib.fa_device_status.argtypes = [i, i]
         lib.fa_set_wait_timeout_ns.restype = ctypes.c_ulonglong
         lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        lib.fa_set_stall_probe.restype = i
+        lib.fa_set_stall_probe.argtypes = [i]
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_status_string.argtypes = [i]
         lib.fa_last_error_message.restype = ctypes.c_char_p
@@ -172,6 +175,11 @@ def device_status(device: int | None = None, clear: bool = True) -> int:
 def set_wait_timeout_ns(ns: int) -> int:
     """Set the kernels' bounded-wait limit (0 restores the default); returns the old one."""
     return int(load_library().fa_set_wait_timeout_ns(int(ns)))
+
+
+def set_stall_probe(enable: bool) -> bool:
+    """Test hook: make subsequent bf16 launches take their time-out path."""
+    return bool(load_library().fa_set_stall_probe(int(bool(enable))))
 
 
 def version() -> int:

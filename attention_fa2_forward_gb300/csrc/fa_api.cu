@@ -24,6 +24,7 @@ constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
 std::mutex g_mutex;
 unsigned* g_status[kMaxDevices] = {};
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int> g_stall_probe{0};
 thread_local char t_message[512] = "";
 
 fa_status_t fail(fa_status_t st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
@@ -164,6 +165,7 @@ fa_status_t fa_mha_no_cache(void* out, float* lse, const void* q, const void* k,
   p.lse = lse;
   p.status = status;
   p.wait_limit_ns = g_wait_limit_ns.load();
+  p.stall_probe = g_stall_probe.load();
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == FA_DTYPE_BF16) {
@@ -215,6 +217,8 @@ fa_status_t fa_device_status(int device, int clear) {
 unsigned long long fa_set_wait_timeout_ns(unsigned long long ns) {
   return g_wait_limit_ns.exchange(ns == 0 ? kDefaultWaitLimitNs : ns);
 }
+
+int fa_set_stall_probe(int enable) { return g_stall_probe.exchange(enable ? 1 : 0); }
 
 const char* fa_status_string(int status) {
   switch (status) {

@@ -229,6 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, D, false, true);
       bool ok = true;
+      // Test hook: wait on the drain barrier, which nothing signals before
+      // this thread's own final commit, so the bounded wait must expire.
+      if (p.stall_probe && !ptx::mbar_wait(bar_drain, 0, limit)) {
+        fail();
+        ok = false;
+      }
 #pragma unroll
       for (int t = 0; t < kQTiles; ++t)
         if (ok && lo[t] < hi[t] && !ptx::mbar_wait(bar_q_full + 8 * t, 0, limit)) {

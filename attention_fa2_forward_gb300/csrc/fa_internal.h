@@ -22,6 +22,7 @@ struct FwdProblem {
   float* lse;            // [B, H, S] fp32 or nullptr
   unsigned* status;      // device status word (sticky error bits)
   unsigned long long wait_limit_ns;
+  int stall_probe;       // test hook: the MMA issuer first waits on a barrier nothing signals
 };
 
 // Tensor-core (tcgen05) bf16 forward. q/k/v/out are device pointers to

@@ -56,7 +56,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+    if ((it & 7u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

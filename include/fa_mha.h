@@ -95,6 +95,17 @@ fa_status_t fa_device_status(int device, int clear);
  */
 unsigned long long fa_set_wait_timeout_ns(unsigned long long ns);
 
+/*
+ * fa_set_stall_probe -- test hook for the time-out path. While enabled, the
+ * MMA-issuing thread of every bf16 launch first waits on a barrier that
+ * nothing signals; that wait ends when the bounded-wait limit expires, so
+ * every CTA takes its time-out path (records FA_ERR_TIMEOUT, drains its own
+ * copies, frees tensor memory, returns) and the outputs are undefined. The
+ * launch still completes and the context stays usable. Affects launches made
+ * after the call; returns the previous setting (0 or 1).
+ */
+int fa_set_stall_probe(int enable);
+
 /* fa_status_string -- a static, human-readable name for a status code. */
 const char *fa_status_string(int status);
 

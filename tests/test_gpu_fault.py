@@ -1,0 +1,45 @@
+"""Failure detection without a GPU fault: the kernels' spin-waits are bounded.
+
+The stall probe makes the MMA-issuing thread of each CTA wait on a barrier
+that nothing signals. With a 20 ms wait limit that wait expires; every CTA
+must then record the time-out in the device status word, stop issuing, drain
+its own TMA copies and MMAs, free its tensor memory and return. The call
+completes, fa_device_status reports FA_ERR_TIMEOUT, and the context stays
+usable: a following call without the probe is correct.
+"""
+import math
+
+import pytest
+import torch
+
+import attention_fa2_forward_gb300 as fa
+from attention_fa2_forward_gb300.inputs import make_qkv
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_timeout_is_reported_and_recoverable(oracle_mod):
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    fa.build()
+    dev = torch.device("cuda:0")
+    q, k, v = make_qkv(1, 1024, 8, 2, 128, torch.bfloat16, seed=21)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    scale = 1.0 / math.sqrt(128)
+    fa.mha_no_cache(qd, kd, vd, scale, "causal")
+    assert fa.device_status(clear=True) == fa.FA_OK
+    old = fa.set_wait_timeout_ns(20_000_000)
+    fa.set_stall_probe(True)
+    try:
+        fa.mha_no_cache(qd, kd, vd, scale, "causal")
+        assert fa.device_status(clear=True) == fa.FA_ERR_TIMEOUT
+    finally:
+        fa.set_stall_probe(False)
+        fa.set_wait_timeout_ns(old)
+    assert fa.device_status(clear=True) == fa.FA_OK
+    out = fa.mha_no_cache(qd, kd, vd, scale, "causal")
+    torch.cuda.synchronize()
+    ref, _ = oracle_mod.mha_forward(q, k, v, scale, True, -1)
+    err = (out.double().cpu() - torch.from_numpy(ref)).abs()
+    assert err.max().item() <= 2e-2 and err.mean().item() <= 2e-3
+    assert fa.device_status() == fa.FA_OK
