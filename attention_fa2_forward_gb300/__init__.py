@@ -35,7 +35,7 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 
 # Every symbol the header declares (checked by the tests).
-EXPORTS = ("fa_mha_no_cache", "fa_device_status",
+EXPORTS = ("fa_mha_no_cache", "fa_mha_no_cache_noalloc", "fa_device_status",
            "fa_set_wait_timeout_ns", "fa_set_stall_probe", "fa_status_string",
            "fa_last_error_message", "fa_version", "fa_shutdown")
 

@@ -83,6 +83,8 @@ fa_status_t device_status_word(int dev, unsigned** out) {
 
 namespace fa {
 
+void record_error_message(const char* msg) { snprintf(t_message, sizeof(t_message), "%s", msg); }
+
 bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;

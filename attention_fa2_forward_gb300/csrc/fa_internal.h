@@ -34,6 +34,9 @@ cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, co
 cudaError_t launch_fwd_f32_simt(const FwdProblem& p, float* out, const float* q, const float* k,
                                 const float* v, cudaStream_t stream);
 
+// Stores `msg` as the calling thread's fa_last_error_message().
+void record_error_message(const char* msg);
+
 // Encodes a 4-D BSHD tensor map (dims D, heads, S, B) for bf16 data with a
 // {64, 1, 128, 1} box and 128-byte swizzle. Returns false on failure.
 bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D);

@@ -81,6 +81,39 @@ fa_status_t fa_mha_no_cache(void *out, float *lse, const void *q, const void *k,
                             int local_window_size, int dtype, void *stream);
 
 /*
+ * fa_mha_no_cache_noalloc -- the same bf16 attention forward as
+ * fa_mha_no_cache, for callers that cannot allocate device memory. The pages
+ * describe nothing like it; it exists for code that does not own the CUDA
+ * allocator (a framework's caching allocator or a pool sized up front),
+ * must not allocate on a latency-critical path, or must account for every
+ * allocation before it starts.
+ *
+ * It calls no cudaMalloc, cudaFree or other allocating routine. The one
+ * piece of global memory the kernel needs besides its inputs and outputs (a
+ * 4-byte status word) lives in a 256-byte array inside this library that
+ * every GPU loading the library holds until the process exits; sizes that
+ * would need more scratch than that are rejected with FA_ERR_UNSUPPORTED
+ * (the status word does not grow with B, S, H or D, so every size accepted
+ * by fa_mha_no_cache fits).
+ *
+ * Arguments are those of fa_mha_no_cache for dtype FA_DTYPE_BF16 (the only
+ * dtype it takes), plus check_status: when non-zero the call synchronises
+ * `stream` after the launch and returns FA_ERR_TIMEOUT if the kernel gave up
+ * on a bounded wait (default 2 s limit); when zero it returns right after the
+ * launch. Each call clears the status word on `stream` before its launch.
+ *
+ * The first call on each device resolves the array's device address (a
+ * cudaGetSymbolAddress set-up step); make that first call before any stream
+ * capture. All calls share the one array: calls that overlap on the GPU (on
+ * different streams) race on the status word, so one call may report or hide
+ * another's time-out.
+ */
+fa_status_t fa_mha_no_cache_noalloc(void *out, float *lse, const void *q, const void *k,
+                                    const void *v, int B, int S, int H, int Hkv, int D,
+                                    float scale, int mask_kind, int local_window_size,
+                                    void *stream, int check_status);
+
+/*
  * fa_device_status -- synchronises `device` (cudaDeviceSynchronize) and reads
  * its sticky status word: FA_OK, or FA_ERR_TIMEOUT if any kernel since the
  * last clear abandoned a bounded wait. With clear != 0 the word is reset.
