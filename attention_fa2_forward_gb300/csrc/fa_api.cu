@@ -12,7 +12,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/fa_mha.h"
+#include "fa_mha.h"
 #include "fa_internal.h"
 
 namespace {

@@ -73,6 +73,35 @@ struct Cfg {
   static constexpr uint32_t kColO = 256;                   // O_t at kColO + t * D
 };
 
+// Pairs of score columns whose exponential runs on the FMA pipe (a degree-3
+// polynomial) instead of the MUFU unit: kPolyPer8 of every 8 pairs, spread
+// evenly. The MUFU unit (16 exp2 per clock per SM) is as busy as the tensor
+// core without this; the split balances MUFU and FMA-pipe issue.
+constexpr int kPolyPer8 = 0;
+__host__ __device__ constexpr bool poly_pair(int i) {
+  return ((i & 7) * kPolyPer8) / 8 != (((i & 7) + 1) * kPolyPer8) / 8;
+}
+
+constexpr uint32_t kNegInfBits = 0xff800000u;
+
+// Hides (-inf) the scores outside the visible key columns [vlo, vhi] of the
+// tile; with a zero scale the visible ones become 0 (the caller then uses 1
+// as the multiplier, which keeps -inf * 0 out of the hidden lanes).
+// Branch-free: one unsigned range test and two selects per element.
+__device__ __forceinline__ void mask_tile(uint32_t* r, int vlo, int vhi, bool zero_scale) {
+  int lo = max(vlo, 0);
+  const int hi = min(vhi, kBN - 1);
+  unsigned span = static_cast<unsigned>(hi - lo);
+  if (hi < lo) {  // nothing visible in this tile
+    lo = 2 * kBN;
+    span = 0;
+  }
+  const uint32_t keep = zero_scale ? 0u : 0xffffffffu;
+#pragma unroll
+  for (int e = 0; e < kBN; ++e)
+    r[e] = static_cast<unsigned>(e - lo) <= span ? (r[e] & keep) : kNegInfBits;
+}
+
 // Visibility bounds of query row i (keys lo..hi inclusive may be visible).
 struct RowBounds {
   int lo, hi;
@@ -253,28 +282,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         return s;
       };
-      // S_t = Q_t K^T: K-major A (Q) and B (K), K = D in steps of 16.
+      const uint64_t dq0 = ptx::smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dk0 = ptx::smem_desc_sw128(sKV, 16, 1024);
+      const uint64_t dv0 = ptx::smem_desc_sw128(sKV, kBoxBytes, 1024);
       auto issue_s = [&](int t, int kslot) {
-        const uint32_t qa = sQ + t * C::kTileBytes;
-        const uint32_t kb = sKV + kslot * C::kTileBytes;
+        const uint64_t dq = dq0 + static_cast<uint32_t>((t * C::kTileBytes) >> 4);
+        const uint64_t dk = dk0 + static_cast<uint32_t>((kslot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          const uint64_t da = ptx::smem_desc_sw128(qa + off, 16, 1024);
-          const uint64_t db = ptx::smem_desc_sw128(kb + off, 16, 1024);
-          ptx::mma_ss(tmem + t * kBN, da, db, kIdescS, kk > 0 ? 1u : 0u);
+          const uint32_t off = static_cast<uint32_t>(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+          ptx::mma_ss(tmem + t * kBN, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
         }
         ptx::tc_commit(bar_s_full + 8 * t);
       };
-      // O_t (+)= P_t V: A = P_t from tensor memory, B = V (MN-major, N = D).
       auto issue_pv = [&](int t, int vslot, bool accumulate) {
-        const uint32_t vb = sKV + vslot * C::kTileBytes;
+        const uint64_t dv = dv0 + static_cast<uint32_t>((vslot * C::kTileBytes) >> 4);
+        const uint32_t acc = accumulate ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t dv = ptx::smem_desc_sw128(vb + kk * 2048, kBoxBytes, 1024);
-          ptx::mma_ts(tmem + C::kColO + t * D, tmem + t * kBN + kk * 8, dv, kIdescPV,
-                      (accumulate || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          ptx::mma_ts(tmem + C::kColO + t * D, tmem + t * kBN + kk * 8,
+                      dv + static_cast<uint32_t>(kk * 128), kIdescPV, kk > 0 ? 1u : acc);
       };
       uint32_t p_phase[kQTiles] = {0u, 0u};
       auto wait_p = [&](int t) -> bool {
@@ -345,6 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_base + C::kColO + t * D;
     const float c = p.scale_log2;
     const RowBounds rb = row_bounds(p, i);
+    // A zero scale makes every visible score 0: use 0 as the score and 1 as
+    // the multiplier.
+    const bool zero_scale = !(c > 0.f);
+    const float ce = zero_scale ? 1.f : c;
 
     float m_use = -INFINITY;  // running max of score * scale * log2(e) (possibly stale)
     float l_run = 0.f;        // running sum of 2^(x - m_use)
@@ -374,27 +405,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int vlo = rb.lo == INT_MIN ? INT_MIN : rb.lo - k0;
       const int vhi = rb.hi - k0;
 
-      // Row maximum of the visible raw scores.
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-      if (full) {
+      // Tiles that straddle the mask boundary (or a zero scale): hide the
+      // invisible scores in place, then every tile takes the same path.
+      if (!full || zero_scale) mask_tile(r, vlo, vhi, zero_scale);
+
+      // Row maximum of the (visible) scores.
+      float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < kBN; e += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(r[e]));
-          mx1 = fmaxf(mx1, __uint_as_float(r[e + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(r[e + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(r[e + 3]));
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < kBN; e += 4) {
-          mx0 = fmaxf(mx0, (e >= vlo && e <= vhi) ? __uint_as_float(r[e]) : -INFINITY);
-          mx1 = fmaxf(mx1, (e + 1 >= vlo && e + 1 <= vhi) ? __uint_as_float(r[e + 1]) : -INFINITY);
-          mx2 = fmaxf(mx2, (e + 2 >= vlo && e + 2 <= vhi) ? __uint_as_float(r[e + 2]) : -INFINITY);
-          mx3 = fmaxf(mx3, (e + 3 >= vlo && e + 3 <= vhi) ? __uint_as_float(r[e + 3]) : -INFINITY);
-        }
+      for (int e = 0; e < kBN; e += 8) {
+        a0 = ptx::max3(a0, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+        a1 = ptx::max3(a1, __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+        a2 = ptx::max3(a2, __uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
+        a3 = ptx::max3(a3, __uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      const float m_tile = mx == -INFINITY ? -INFINITY : mx * c;  // scale >= 0
+      const float mx = ptx::max3(a0, a1, fmaxf(a2, a3));
+      const float m_tile = mx == -INFINITY ? -INFINITY : mx * ce;
       const float m_new = fmaxf(m_use, m_tile);
       const bool first = j == tlo;
       float alpha = 1.f;
@@ -408,42 +433,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float neg_base = m_use == -INFINITY ? 0.f : -m_use;
 
-      // P = 2^(x - m_use), row sum, and bf16 pairs written over S.
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      if (full) {
+      // P = 2^(x - m_use) (hidden scores are -inf and give 0), row sum, and
+      // bf16 pairs written over S. Pairs of columns: x = s * c - m with packed
+      // FMAs; kPolyPer8 of every 8 pairs take 2^x on the FMA pipe.
+      float row_sum;
+      {
+        const uint64_t c2 = ptx::pair(__float_as_uint(ce), __float_as_uint(ce));
+        const uint64_t nb2 = ptx::pair(__float_as_uint(neg_base), __float_as_uint(neg_base));
+        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
 #pragma unroll
-        for (int e = 0; e < kBN; e += 4) {
-          const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(r[e]), c, neg_base));
-          const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 1]), c, neg_base));
-          const float p2 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 2]), c, neg_base));
-          const float p3 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 3]), c, neg_base));
-          s0 += p0;
-          s1 += p1;
-          s2 += p2;
-          s3 += p3;
-          r[e / 2] = ptx::pack_bf16x2(p0, p1);
-          r[e / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+        for (int i = 0; i < kBN / 2; ++i) {
+          uint32_t lo, hi;
+          ptx::unpair(ptx::fma2(ptx::pair(r[2 * i], r[2 * i + 1]), c2, nb2), lo, hi);
+          if (poly_pair(i)) {
+            ptx::exp2_poly3_pair(lo, hi);
+          } else {
+            lo = __float_as_uint(ptx::ex2_approx(__uint_as_float(lo)));
+            hi = __float_as_uint(ptx::ex2_approx(__uint_as_float(hi)));
+          }
+          const uint64_t pp = ptx::pair(lo, hi);
+          if ((i & 3) == 0) acc0 = ptx::add2(acc0, pp);
+          if ((i & 3) == 1) acc1 = ptx::add2(acc1, pp);
+          if ((i & 3) == 2) acc2 = ptx::add2(acc2, pp);
+          if ((i & 3) == 3) acc3 = ptx::add2(acc3, pp);
+          r[i] = ptx::pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
         }
-      } else {
-#pragma unroll
-        for (int e = 0; e < kBN; e += 4) {
-          float p0 = ptx::ex2_approx(fmaf(__uint_as_float(r[e]), c, neg_base));
-          float p1 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 1]), c, neg_base));
-          float p2 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 2]), c, neg_base));
-          float p3 = ptx::ex2_approx(fmaf(__uint_as_float(r[e + 3]), c, neg_base));
-          p0 = (e >= vlo && e <= vhi) ? p0 : 0.f;
-          p1 = (e + 1 >= vlo && e + 1 <= vhi) ? p1 : 0.f;
-          p2 = (e + 2 >= vlo && e + 2 <= vhi) ? p2 : 0.f;
-          p3 = (e + 3 >= vlo && e + 3 <= vhi) ? p3 : 0.f;
-          s0 += p0;
-          s1 += p1;
-          s2 += p2;
-          s3 += p3;
-          r[e / 2] = ptx::pack_bf16x2(p0, p1);
-          r[e / 2 + 1] = ptx::pack_bf16x2(p2, p3);
-        }
+        uint32_t u0, u1;
+        ptx::unpair(ptx::add2(ptx::add2(acc0, acc1), ptx::add2(acc2, acc3)), u0, u1);
+        row_sum = __uint_as_float(u0) + __uint_as_float(u1);
       }
-      l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
+      l_run = l_run * alpha + row_sum;
 #pragma unroll
       for (int c0 = 0; c0 < kBN / 2; c0 += 32) ptx::tmem_st_32x32b_x32(tS + c0, r + c0);
 

@@ -20,7 +20,7 @@
 #include <cstdio>
 #include <mutex>
 
-#include "../../include/fa_mha.h"
+#include "fa_mha.h"
 #include "fa_internal.h"
 
 namespace {
