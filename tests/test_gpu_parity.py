@@ -170,3 +170,19 @@ def test_deterministic_and_stream_aware(oracle_mod):
     s.synchronize()
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def test_ragged_long_window_sampled_rows(oracle_mod):
+    """A long sequence that is not a multiple of the 256-row block, sliding window."""
+    B, S, H, Hkv, D, W = 1, 5000, 8, 2, 128, 1000
+    q, k, v = make_qkv(B, S, H, Hkv, D, torch.bfloat16, seed=31)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = _run_gpu(q, k, v, scale, True, W)
+    rows = _sample_rows(S, 31)
+    ref_out, ref_lse = oracle_mod.mha_forward(q[:, rows], k, v, scale, True, W, rows=rows)
+    _compare(out[:, rows], lse[:, :, rows], ref_out, ref_lse, torch.bfloat16, "S5000 W1000")
+    assert np.isfinite(out).all()
+
+
+def test_ragged_noncausal_whole(oracle_mod):
+    _full_case(oracle_mod, 1, 3000, 4, 4, 64, torch.bfloat16, False, -1, seed=32)
