@@ -35,7 +35,8 @@ FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 
 # Every symbol the header declares (checked by the tests).
-EXPORTS = ("fa_mha_no_cache", "fa_mha_no_cache_noalloc", "fa_device_status",
+EXPORTS = ("fa_mha_no_cache", "fa_mha_no_cache_strided", "fa_mha_no_cache_noalloc",
+           "fa_device_status",
            "fa_set_wait_timeout_ns", "fa_set_stall_probe", "fa_status_string",
            "fa_last_error_message", "fa_version", "fa_shutdown")
 
@@ -65,6 +66,10 @@ def load_library(path: str | None = None):
         lib.fa_mha_no_cache.restype = i
         lib.fa_mha_no_cache.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float,
                                         i, i, i, vp]
+        lp = ctypes.POINTER(ctypes.c_longlong)
+        lib.fa_mha_no_cache_strided.restype = i
+        lib.fa_mha_no_cache_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, lp, lp, lp, lp,
+                                                ctypes.c_float, i, i, i, vp]
         lib.fa_device_status.restype = i
         lib.fa_device_status.argtypes = [i, i]
         lib.fa_set_wait_timeout_ns.restype = ctypes.c_ulonglong
@@ -119,10 +124,12 @@ def mha_no_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float
                  stream: torch.cuda.Stream | None = None):
     """Fused attention forward (``mo.mha.no_cache``) on the current CUDA device.
 
-    q: [B, S, H, D]; k, v: [B, S, Hkv, D]; all contiguous CUDA tensors of one
-    dtype (bf16 or fp32). ``scale`` defaults to 1/sqrt(D). ``mask`` is "none"
-    or "causal"; ``window`` > 0 adds a sliding window (causal only). Returns
-    out [B, S, H, D] (q's dtype), and lse [B, H, S] fp32 if ``return_lse``.
+    q: [B, S, H, D]; k, v: [B, S, Hkv, D]; CUDA tensors of one dtype (bf16 or
+    fp32) whose last dimension is contiguous (any other strides are passed to
+    the strided entry point). ``scale`` defaults to 1/sqrt(D). ``mask`` is
+    "none" or "causal"; ``window`` > 0 adds a sliding window (causal only).
+    Returns out [B, S, H, D] (q's dtype), and lse [B, H, S] fp32 if
+    ``return_lse``; a given ``out`` may also be a strided view.
     """
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D (BSHD)")
@@ -134,8 +141,8 @@ def mha_no_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float
     for name, t in (("q", q), ("k", k), ("v", v)):
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous (BSHD, D fastest)")
+        if t.stride(-1) != 1:
+            raise ValueError(f"{name} must have a contiguous last (D) dimension")
         if t.dtype != q.dtype:
             raise TypeError("q, k, v must share one dtype")
         if t.device != q.device:
@@ -145,9 +152,9 @@ def mha_no_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float
         scale = 1.0 / (D ** 0.5)
     if out is None:
         out = torch.empty_like(q)
-    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() \
+    elif out.shape != q.shape or out.dtype != q.dtype or out.stride(-1) != 1 \
             or out.device != q.device:
-        raise ValueError("out must be a contiguous tensor with q's shape, dtype and device")
+        raise ValueError("out must have q's shape, dtype and device and a contiguous last dim")
     if lse is None and return_lse:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
     elif lse is not None and (lse.shape != (B, H, S) or lse.dtype != torch.float32
@@ -156,11 +163,19 @@ def mha_no_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float
     lib = load_library()
     with torch.cuda.device(q.device):
         st = stream if stream is not None else torch.cuda.current_stream(q.device)
-        rc = lib.fa_mha_no_cache(
-            out.data_ptr(), lse.data_ptr() if lse is not None else None,
-            q.data_ptr(), k.data_ptr(), v.data_ptr(),
-            B, S, H, Hkv, D, float(scale), _mask_code(mask), int(window), dtype,
-            st.cuda_stream)
+        lse_ptr = lse.data_ptr() if lse is not None else None
+        if all(t.is_contiguous() for t in (q, k, v, out)):
+            rc = lib.fa_mha_no_cache(
+                out.data_ptr(), lse_ptr, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                B, S, H, Hkv, D, float(scale), _mask_code(mask), int(window), dtype,
+                st.cuda_stream)
+        else:
+            arr = ctypes.c_longlong * 3
+            sq, sk, sv, so = (arr(*t.stride()[:3]) for t in (q, k, v, out))
+            rc = lib.fa_mha_no_cache_strided(
+                out.data_ptr(), lse_ptr, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                B, S, H, Hkv, D, sq, sk, sv, so, float(scale), _mask_code(mask), int(window),
+                dtype, st.cuda_stream)
     _check(rc)
     return (out, lse) if return_lse else out
 

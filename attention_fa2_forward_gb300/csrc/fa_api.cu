@@ -85,14 +85,16 @@ namespace fa {
 
 void record_error_message(const char* msg) { snprintf(t_message, sizeof(t_message), "%s", msg); }
 
-bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D) {
+bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D,
+                            BshdStrides st) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
+  st = resolve_strides(st, S, heads, D);
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
-                                 static_cast<cuuint64_t>(heads) * D * 2,
-                                 static_cast<cuuint64_t>(S) * heads * D * 2};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.h) * 2,
+                                 static_cast<cuuint64_t>(st.s) * 2,
+                                 static_cast<cuuint64_t>(st.b) * 2};
   const cuuint32_t box[4] = {64, 1, 128, 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
@@ -104,11 +106,15 @@ bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, in
 
 }  // namespace fa
 
-extern "C" {
+namespace {
 
-fa_status_t fa_mha_no_cache(void* out, float* lse, const void* q, const void* k, const void* v,
-                            int B, int S, int H, int Hkv, int D, float scale, int mask_kind,
-                            int local_window_size, int dtype, void* stream) {
+// Validates the arguments, then launches the kernel of `dtype` on `stream`.
+// `strides` (may be null: dense) holds the element strides along B, S, H of
+// q, k, v and out, in that order.
+fa_status_t forward(void* out, float* lse, const void* q, const void* k, const void* v, int B,
+                    int S, int H, int Hkv, int D, float scale, int mask_kind,
+                    int local_window_size, int dtype, void* stream,
+                    const fa::BshdStrides* strides) {
   // ---- arguments (no CUDA call before these pass)
   if (out == nullptr || q == nullptr || k == nullptr || v == nullptr)
     return fail(FA_ERR_INVALID_ARG, "null tensor pointer (out=%p q=%p k=%p v=%p)", out, q, k, v);
@@ -140,6 +146,21 @@ fa_status_t fa_mha_no_cache(void* out, float* lse, const void* q, const void* k,
       (lse != nullptr && !aligned(lse, 4)))
     return fail(FA_ERR_UNSUPPORTED, "tensors must be %u-byte aligned",
                 static_cast<unsigned>(need));
+  if (strides != nullptr) {
+    static const char* const names[4] = {"q", "k", "v", "out"};
+    for (int t = 0; t < 4; ++t) {
+      const fa::BshdStrides& st = strides[t];
+      if (st.b < 1 || st.s < 1 || st.h < 1)
+        return fail(FA_ERR_INVALID_ARG, "%s strides must be >= 1 (got %lld, %lld, %lld)",
+                    names[t], st.b, st.s, st.h);
+      if (st.b >= (1ll << 38) || st.s >= (1ll << 38) || st.h >= (1ll << 38))
+        return fail(FA_ERR_UNSUPPORTED, "%s strides too large", names[t]);
+      if (dtype == FA_DTYPE_BF16 && (st.b % 8 || st.s % 8 || st.h % 8))
+        return fail(FA_ERR_UNSUPPORTED,
+                    "bf16 %s strides must be multiples of 8 elements (16 bytes) for TMA",
+                    names[t]);
+    }
+  }
 
   // ---- device
   int dev = 0;
@@ -168,6 +189,12 @@ fa_status_t fa_mha_no_cache(void* out, float* lse, const void* q, const void* k,
   p.status = status;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.stall_probe = g_stall_probe.load();
+  if (strides != nullptr) {
+    p.sq = strides[0];
+    p.sk = strides[1];
+    p.sv = strides[2];
+    p.so = strides[3];
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == FA_DTYPE_BF16) {
@@ -179,6 +206,37 @@ fa_status_t fa_mha_no_cache(void* out, float* lse, const void* q, const void* k,
     if (err != cudaSuccess) return cuda_fail(err, "fp32 kernel launch");
   }
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_mha_no_cache(void* out, float* lse, const void* q, const void* k, const void* v,
+                            int B, int S, int H, int Hkv, int D, float scale, int mask_kind,
+                            int local_window_size, int dtype, void* stream) {
+  return forward(out, lse, q, k, v, B, S, H, Hkv, D, scale, mask_kind, local_window_size, dtype,
+                 stream, nullptr);
+}
+
+fa_status_t fa_mha_no_cache_strided(void* out, float* lse, const void* q, const void* k,
+                                    const void* v, int B, int S, int H, int Hkv, int D,
+                                    const long long* q_strides, const long long* k_strides,
+                                    const long long* v_strides, const long long* out_strides,
+                                    float scale, int mask_kind, int local_window_size, int dtype,
+                                    void* stream) {
+  if (q_strides == nullptr || k_strides == nullptr || v_strides == nullptr ||
+      out_strides == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "null stride array");
+  const long long* in[4] = {q_strides, k_strides, v_strides, out_strides};
+  fa::BshdStrides st[4];
+  for (int t = 0; t < 4; ++t) {
+    st[t].b = in[t][0];
+    st[t].s = in[t][1];
+    st[t].h = in[t][2];
+  }
+  return forward(out, lse, q, k, v, B, S, H, Hkv, D, scale, mask_kind, local_window_size, dtype,
+                 stream, st);
 }
 
 fa_status_t fa_device_status(int device, int clear) {

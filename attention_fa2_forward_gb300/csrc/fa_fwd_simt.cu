@@ -36,7 +36,8 @@ template <int D>
 __global__ void __launch_bounds__(kRows * 32)
     fa_fwd_f32_simt_kernel(const float* __restrict__ q, const float* __restrict__ k,
                            const float* __restrict__ v, float* __restrict__ out,
-                           const FwdProblem p) {
+                           const FwdProblem p, BshdStrides sq, BshdStrides sk, BshdStrides sv,
+                           BshdStrides so) {
   constexpr int kPerLane = D / 32;
   __shared__ float sK[kKeys][D + 1];
   __shared__ float sV[kKeys][D];
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(kRows * 32)
   const bool row_valid = i < p.S;
 
   for (int d = lane; d < D; d += 32)
-    sQ[warp][d] = row_valid ? q[((static_cast<size_t>(b) * p.S + i) * p.H + h) * D + d] : 0.f;
+    sQ[warp][d] = row_valid ? q[b * sq.b + i * sq.s + h * sq.h + d] : 0.f;
 
   // Keys any row of this CTA may see, and the ones row i sees.
   const int r_last = min(r0 + kRows, p.S) - 1;
@@ -73,9 +74,8 @@ __global__ void __launch_bounds__(kRows * 32)
       const int key = k0 + kr;
       float kval = 0.f, vval = 0.f;
       if (key < kv_end) {
-        const size_t off = ((static_cast<size_t>(b) * p.S + key) * p.Hkv + hk) * D + d;
-        kval = k[off];
-        vval = v[off];
+        kval = k[b * sk.b + key * sk.s + hk * sk.h + d];
+        vval = v[b * sv.b + key * sv.s + hk * sv.h + d];
       }
       sK[kr][d] = kval;
       sV[kr][d] = vval;
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kRows * 32)
 
   if (row_valid) {
     const float inv_l = 1.f / l;
-    float* orow = out + ((static_cast<size_t>(b) * p.S + i) * p.H + h) * D;
+    float* orow = out + (b * so.b + i * so.s + h * so.h);
 #pragma unroll
     for (int u = 0; u < kPerLane; ++u) orow[lane + 32 * u] = o[u] * inv_l;
     if (p.lse != nullptr && lane == 0)
@@ -121,7 +121,9 @@ cudaError_t launch_d(const FwdProblem& p, float* out, const float* q, const floa
                      const float* v, cudaStream_t stream) {
   const dim3 grid((p.S + kRows - 1) / kRows, p.H, p.B);
   if (grid.y > 65535u || grid.z > 65535u) return cudaErrorInvalidConfiguration;
-  fa_fwd_f32_simt_kernel<D><<<grid, kRows * 32, 0, stream>>>(q, k, v, out, p);
+  fa_fwd_f32_simt_kernel<D><<<grid, kRows * 32, 0, stream>>>(
+      q, k, v, out, p, resolve_strides(p.sq, p.S, p.H, D), resolve_strides(p.sk, p.S, p.Hkv, D),
+      resolve_strides(p.sv, p.S, p.Hkv, D), resolve_strides(p.so, p.S, p.H, D));
   return cudaGetLastError();
 }
 

@@ -552,10 +552,10 @@ template <int D>
 cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* k, const void* v,
                      cudaStream_t stream) {
   CUtensorMap tq, tk, tv, to;
-  if (!encode_bshd_tensor_map(&tq, q, p.B, p.S, p.H, D) ||
-      !encode_bshd_tensor_map(&tk, k, p.B, p.S, p.Hkv, D) ||
-      !encode_bshd_tensor_map(&tv, v, p.B, p.S, p.Hkv, D) ||
-      !encode_bshd_tensor_map(&to, out, p.B, p.S, p.H, D))
+  if (!encode_bshd_tensor_map(&tq, q, p.B, p.S, p.H, D, p.sq) ||
+      !encode_bshd_tensor_map(&tk, k, p.B, p.S, p.Hkv, D, p.sk) ||
+      !encode_bshd_tensor_map(&tv, v, p.B, p.S, p.Hkv, D, p.sv) ||
+      !encode_bshd_tensor_map(&to, out, p.B, p.S, p.H, D, p.so))
     return cudaErrorInvalidValue;
   const int nqb = (p.S + kQTiles * kBM - 1) / (kQTiles * kBM);
   const long long grid = static_cast<long long>(nqb) * p.H * p.B;

@@ -12,6 +12,22 @@ namespace fa {
 // Bits of the per-device status word the kernels may set.
 constexpr unsigned kStatusWaitTimeout = 1u;
 
+// Element strides of a BSHD (or BShD) view along B, S and H; D is
+// contiguous. All zero means the dense layout of the view's shape.
+struct BshdStrides {
+  long long b = 0, s = 0, h = 0;
+};
+
+// The dense strides when `st` is all zero, else `st`.
+inline BshdStrides resolve_strides(BshdStrides st, int S, int heads, int D) {
+  if (st.b == 0 && st.s == 0 && st.h == 0) {
+    st.h = D;
+    st.s = static_cast<long long>(heads) * D;
+    st.b = static_cast<long long>(S) * heads * D;
+  }
+  return st;
+}
+
 // Problem description handed to both kernels by value.
 struct FwdProblem {
   int B, S, H, Hkv, D;
@@ -23,6 +39,7 @@ struct FwdProblem {
   unsigned* status;      // device status word (sticky error bits)
   unsigned long long wait_limit_ns;
   int stall_probe;       // test hook: the MMA issuer first waits on a barrier nothing signals
+  BshdStrides sq, sk, sv, so;  // layouts of q, k, v, out (zero: dense)
 };
 
 // Tensor-core (tcgen05) bf16 forward. q/k/v/out are device pointers to
@@ -37,8 +54,10 @@ cudaError_t launch_fwd_f32_simt(const FwdProblem& p, float* out, const float* q,
 // Stores `msg` as the calling thread's fa_last_error_message().
 void record_error_message(const char* msg);
 
-// Encodes a 4-D BSHD tensor map (dims D, heads, S, B) for bf16 data with a
-// {64, 1, 128, 1} box and 128-byte swizzle. Returns false on failure.
-bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D);
+// Encodes a 4-D BSHD tensor map (dims D, heads, S, B; element strides `st`,
+// D contiguous) for bf16 data with a {64, 1, 128, 1} box and 128-byte
+// swizzle. Returns false on failure.
+bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D,
+                            BshdStrides st);
 
 }  // namespace fa

@@ -81,6 +81,26 @@ fa_status_t fa_mha_no_cache(void *out, float *lse, const void *q, const void *k,
                             int local_window_size, int dtype, void *stream);
 
 /*
+ * fa_mha_no_cache_strided -- fa_mha_no_cache on strided views: each of q, k,
+ * v and out may be any BSHD view whose D dimension is contiguous, e.g. slices
+ * of a packed [B, S, H + 2 Hkv, D] QKV projection, or a [B, H, S, D] tensor
+ * viewed as BSHD (the Step 0 / Step 4 transposes of the FlashAttentionGPU
+ * page then cost nothing: the kernels address the views directly).
+ *
+ *   x_strides : 3 element strides of that tensor along B, S and H (all >= 1;
+ *               for FA_DTYPE_BF16 multiples of 8 elements, i.e. 16 bytes, as
+ *               TMA requires).
+ * Every other argument, the lse layout ([B, H, S], dense) and the behaviour
+ * are those of fa_mha_no_cache. out must not overlap q, k or v.
+ */
+fa_status_t fa_mha_no_cache_strided(void *out, float *lse, const void *q, const void *k,
+                                    const void *v, int B, int S, int H, int Hkv, int D,
+                                    const long long *q_strides, const long long *k_strides,
+                                    const long long *v_strides, const long long *out_strides,
+                                    float scale, int mask_kind, int local_window_size, int dtype,
+                                    void *stream);
+
+/*
  * fa_mha_no_cache_noalloc -- the same bf16 attention forward as
  * fa_mha_no_cache, for callers that cannot allocate device memory. The pages
  * describe nothing like it; it exists for code that does not own the CUDA

@@ -85,3 +85,25 @@ def test_python_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 4, 2, 64)
     with pytest.raises(ValueError):
         fa.mha_no_cache(q, q, q)
+
+
+def _call_strided(lib, strides=((64, 32, 16),) * 4, q=P, dtype=0, null=None):
+    arr = ctypes.c_longlong * 3
+    st = [arr(*s) for s in strides]
+    if null is not None:
+        st[null] = None
+    return lib.fa_mha_no_cache_strided(P, None, q, P, P, 1, 8, 2, 2, 64, st[0], st[1], st[2],
+                                       st[3], 0.125, 1, -1, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(null=0), fa.FA_ERR_INVALID_ARG),
+    (dict(null=3), fa.FA_ERR_INVALID_ARG),
+    (dict(strides=((64, 32, 16),) * 3 + ((64, 0, 16),)), fa.FA_ERR_INVALID_ARG),
+    (dict(strides=((64, 32, -16),) + ((64, 32, 16),) * 3), fa.FA_ERR_INVALID_ARG),
+    (dict(strides=((64, 36, 16),) + ((64, 32, 16),) * 3), fa.FA_ERR_UNSUPPORTED),  # bf16: 16 B
+    (dict(strides=((1 << 40, 32, 16),) * 4), fa.FA_ERR_UNSUPPORTED),
+])
+def test_strided_validation_happens_before_cuda(lib, kw, code):
+    assert _call_strided(lib, **kw) == code
+    assert lib.fa_last_error_message()

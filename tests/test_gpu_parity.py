@@ -186,3 +186,44 @@ def test_ragged_long_window_sampled_rows(oracle_mod):
 
 def test_ragged_noncausal_whole(oracle_mod):
     _full_case(oracle_mod, 1, 3000, 4, 4, 64, torch.bfloat16, False, -1, seed=32)
+
+
+# --- strided views (fa_mha_no_cache_strided) ------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_packed_qkv_slices_and_strided_output(oracle_mod, dtype):
+    """q, k, v as slices of one packed [B, S, H + 2 Hkv, D] projection; out written
+    into a slice of a wider buffer whose other heads must stay untouched."""
+    B, S, H, Hkv, D = 2, 700, 8, 2, 128
+    q, k, v = make_qkv(B, S, H, Hkv, D, dtype, seed=41)
+    dev = torch.device("cuda:0")
+    qkv = torch.cat([q, k, v], dim=2).to(dev)
+    qs, ks, vs = qkv[:, :, :H], qkv[:, :, H:H + Hkv], qkv[:, :, H + Hkv:]
+    assert not qs.is_contiguous()
+    wide = torch.full((B, S, H + 3, D), float("nan"), dtype=dtype, device=dev)
+    out = wide[:, :, 1:1 + H]
+    scale = 1.0 / math.sqrt(D)
+    _, lse = fa.mha_no_cache(qs, ks, vs, scale, "causal", 300, out=out, return_lse=True)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle_mod.mha_forward(q, k, v, scale, True, 300)
+    _compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse, dtype,
+             f"packed qkv {dtype}")
+    assert torch.isnan(wide[:, :, 0]).all() and torch.isnan(wide[:, :, 1 + H:]).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_bhsd_tensors_viewed_as_bshd(oracle_mod, dtype):
+    """[B, H, S, D] storage read and written through BSHD views."""
+    B, S, H, Hkv, D = 2, 513, 4, 4, 64
+    q, k, v = make_qkv(B, S, H, Hkv, D, dtype, seed=42)
+    dev = torch.device("cuda:0")
+    qv, kv_, vv = (t.permute(0, 2, 1, 3).contiguous().to(dev).permute(0, 2, 1, 3)
+                   for t in (q, k, v))
+    out_store = torch.empty((B, H, S, D), dtype=dtype, device=dev)
+    out = out_store.permute(0, 2, 1, 3)
+    scale = 1.0 / math.sqrt(D)
+    _, lse = fa.mha_no_cache(qv, kv_, vv, scale, "none", out=out, return_lse=True)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle_mod.mha_forward(q, k, v, scale, False, -1)
+    _compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse, dtype,
+             f"bhsd view {dtype}")
