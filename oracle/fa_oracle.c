@@ -27,7 +27,10 @@
  *
  * Mask (the page's `mask_str` / `local_window_size` parameters): key j is
  * visible to query i iff (not causal or j <= i) and (window < 1 or
- * i - j < window). window = -1 (or 0) means no window.
+ * i - j < window) and (causal or window < 1 or j - i < window): a causal
+ * window holds the W keys ending at the query, a window without the causal
+ * mask the keys within distance W - 1 on either side. window = -1 (or 0)
+ * means no window.
  *
  * Everything is fp64. Inputs are fp64 arrays (bf16 / fp32 values widen to
  * fp64 exactly). The score row of one query is materialised (length S); the
@@ -59,6 +62,7 @@ typedef struct {
 static int key_visible(long i, long j, int causal, long window) {
   if (causal && j > i) return 0;
   if (window > 0 && i - j >= window) return 0;
+  if (!causal && window > 0 && j - i >= window) return 0;
   return 1;
 }
 

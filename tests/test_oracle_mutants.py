@@ -22,6 +22,8 @@ MUTANTS = {
     "causal_hides_diagonal": ("if (causal && j > i) return 0;", "if (causal && j >= i) return 0;"),
     "window_one_too_wide": ("if (window > 0 && i - j >= window) return 0;",
                             "if (window > 0 && i - j > window) return 0;"),
+    "two_sided_window_open_right": ("if (!causal && window > 0 && j - i >= window) return 0;",
+                                    "if (!causal && window > 0 && j - i > window) return 0;"),
     "tiled_head_map": ("job->head_map == 0 ? h / G : h % Hkv", "job->head_map == 0 ? h % Hkv : h % Hkv"),
     "scale_dropped": ("score[j] = job->scale * dot;", "score[j] = dot;"),
     "scale_squared": ("score[j] = job->scale * dot;", "score[j] = job->scale * job->scale * dot;"),
@@ -73,7 +75,8 @@ def _pins_fail(oracle_mod, lib):
         lambda: pins.test_single_visible_key_returns_its_value(Bound),
         lambda: pins.test_grouped_equals_explicit_repeat(Bound, True, -1),
     ]
-    for causal, window in [(False, -1), (True, -1), (True, 6)]:
+    checks.append(lambda: pins.test_identical_keys_average_visible_values(Bound, False, 3))
+    for causal, window in [(False, -1), (True, -1), (True, 6), (False, 5)]:
         checks.append(lambda c=causal, w=window: pins.test_matches_torch_sdpa_fp64(Bound, c, w, 2))
     return any(run(c) for c in checks)
 

@@ -28,10 +28,13 @@ def _visible_count(i, S, causal, window):
     hi = i if causal else S - 1
     if window > 0:
         lo = max(0, i - window + 1)
+        if not causal:
+            hi = min(S - 1, i + window - 1)
     return hi - lo + 1
 
 
-MASKS = [(False, -1), (True, -1), (True, 1), (True, 2), (True, 5), (True, 64)]
+MASKS = [(False, -1), (True, -1), (True, 1), (True, 2), (True, 5), (True, 64), (False, 1),
+         (False, 3), (False, 64)]
 
 
 # --- closed forms -----------------------------------------------------------
@@ -60,7 +63,7 @@ def test_identical_keys_average_visible_values(oracle_mod, causal, window):
     out, lse = oracle_mod.mha_forward(q, k, v, scale, causal, window)
     for i in range(S):
         lo = max(0, i - window + 1) if window > 0 else 0
-        hi = i + 1 if causal else S
+        hi = i + 1 if causal else (min(S, i + window) if window > 0 else S)
         n = _visible_count(i, S, causal, window)
         assert hi - lo == n
         for h in range(H):
@@ -241,6 +244,8 @@ def _visible_matrix(S, causal, window):
         vis &= j <= i
     if window > 0:
         vis &= (i - j) < window
+        if not causal:
+            vis &= (j - i) < window
     return vis
 
 
@@ -303,7 +308,8 @@ def _blockwise_normalise_each_step(q, k, v, scale, vis, block_q, block_k):
 
 
 @pytest.mark.parametrize("block", [1, 3, 4, 16])
-@pytest.mark.parametrize("causal,window", [(False, -1), (True, -1), (True, 3), (True, 10)])
+@pytest.mark.parametrize("causal,window", [(False, -1), (True, -1), (True, 3), (True, 10),
+                                           (False, 4)])
 def test_blockwise_online_softmax_agrees(oracle_mod, block, causal, window):
     B, S, H, Hkv, D = 1, 29, 4, 2, 8
     q = _rand((B, S, H, D), 40, 2.0)
@@ -323,7 +329,8 @@ def test_blockwise_online_softmax_agrees(oracle_mod, block, causal, window):
 
 # --- library special case --------------------------------------------------------
 
-@pytest.mark.parametrize("causal,window", [(False, -1), (True, -1), (True, 1), (True, 6)])
+@pytest.mark.parametrize("causal,window", [(False, -1), (True, -1), (True, 1), (True, 6),
+                                           (False, 5)])
 @pytest.mark.parametrize("Hkv", [4, 2, 1])
 def test_matches_torch_sdpa_fp64(oracle_mod, causal, window, Hkv):
     B, S, H, D = 2, 31, 4, 16
