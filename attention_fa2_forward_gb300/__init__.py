@@ -127,7 +127,8 @@ def mha_no_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float
     q: [B, S, H, D]; k, v: [B, S, Hkv, D]; CUDA tensors of one dtype (bf16 or
     fp32) whose last dimension is contiguous (any other strides are passed to
     the strided entry point). ``scale`` defaults to 1/sqrt(D). ``mask`` is
-    "none" or "causal"; ``window`` > 0 adds a sliding window (causal only).
+    "none" or "causal"; ``window`` > 0 adds a sliding window (causal: the W
+    keys ending at the query; none: keys within W - 1 on either side).
     Returns out [B, S, H, D] (q's dtype), and lse [B, H, S] fp32 if
     ``return_lse``; a given ``out`` may also be a strided view.
     """

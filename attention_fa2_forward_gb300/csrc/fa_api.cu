@@ -127,8 +127,6 @@ fa_status_t forward(void* out, float* lse, const void* q, const void* k, const v
   if (local_window_size == 0 || local_window_size < -1)
     return fail(FA_ERR_INVALID_ARG, "local_window_size must be -1 or >= 1 (got %d)",
                 local_window_size);
-  if (local_window_size > 0 && mask_kind != FA_MASK_CAUSAL)
-    return fail(FA_ERR_INVALID_ARG, "a sliding window requires the causal mask");
   if (!std::isfinite(scale))
     return fail(FA_ERR_INVALID_ARG, "scale must be finite");
   if (scale < 0.f)
@@ -182,7 +180,8 @@ fa_status_t forward(void* out, float* lse, const void* q, const void* k, const v
   p.Hkv = Hkv;
   p.D = D;
   p.causal = mask_kind == FA_MASK_CAUSAL ? 1 : 0;
-  p.window = local_window_size > 0 ? local_window_size : 0;
+  // A window of S keys or more hides nothing.
+  p.window = local_window_size > 0 && local_window_size < S ? local_window_size : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.lse = lse;

@@ -58,9 +58,11 @@ __global__ void __launch_bounds__(kRows * 32)
   // Keys any row of this CTA may see, and the ones row i sees.
   const int r_last = min(r0 + kRows, p.S) - 1;
   const int kv_begin = p.window > 0 ? max(0, r0 - p.window + 1) : 0;
-  const int kv_end = p.causal ? r_last + 1 : p.S;
+  const int kv_end =
+      p.causal ? r_last + 1 : (p.window > 0 ? min(p.S, r_last + p.window) : p.S);
   const int vis_lo = p.window > 0 ? i - p.window + 1 : 0;
-  const int vis_hi = p.causal ? min(i, p.S - 1) : p.S - 1;
+  const int vis_hi =
+      p.causal ? min(i, p.S - 1) : (p.window > 0 ? min(i + p.window - 1, p.S - 1) : p.S - 1);
 
   float m = -INFINITY, l = 0.f;
   float o[kPerLane];

@@ -110,7 +110,7 @@ struct RowBounds {
 __device__ __forceinline__ RowBounds row_bounds(const FwdProblem& p, int i) {
   RowBounds r;
   r.lo = p.window > 0 ? i - p.window + 1 : INT_MIN;
-  r.hi = p.causal ? min(i, p.S - 1) : p.S - 1;
+  r.hi = p.causal ? min(i, p.S - 1) : (p.window > 0 ? min(i + p.window - 1, p.S - 1) : p.S - 1);
   return r;
 }
 
@@ -157,7 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int t = 0; t < kQTiles; ++t) {
     q0[t] = qb * (kQTiles * kBM) + t * kBM;
     if (q0[t] < p.S) {
-      const int kv_end = p.causal ? min(p.S, q0[t] + kBM) : p.S;
+      // Window without the causal mask: keys up to the last row + W - 1.
+      const int kv_end = p.causal ? min(p.S, q0[t] + kBM)
+                                  : (p.window > 0 ? min(p.S, q0[t] + kBM - 1 + p.window) : p.S);
       const int kv_begin = p.window > 0 ? max(0, q0[t] - p.window + 1) : 0;
       lo[t] = kv_begin / kBN;
       hi[t] = (kv_end + kBN - 1) / kBN;
@@ -402,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool full = k0 + kBN <= p.S;
       if (p.causal) full = full && (k0 + kBN - 1 <= tq0);
       if (p.window > 0) full = full && (tq0 + kBM - 1 - k0 < p.window);
+      if (p.window > 0 && !p.causal) full = full && (k0 + kBN - 1 - tq0 < p.window);
       const int vlo = rb.lo == INT_MIN ? INT_MIN : rb.lo - k0;
       const int vhi = rb.hi - k0;
 

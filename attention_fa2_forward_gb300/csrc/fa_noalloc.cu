@@ -83,8 +83,7 @@ extern "C" fa_status_t fa_mha_no_cache_noalloc(void* out, float* lse, const void
     return noalloc_fail(FA_ERR_INVALID_ARG, "bad sizes B=%d S=%d H=%d Hkv=%d", B, S, H, Hkv);
   if (mask_kind != FA_MASK_NONE && mask_kind != FA_MASK_CAUSAL)
     return noalloc_fail(FA_ERR_INVALID_ARG, "unknown mask kind %d", mask_kind);
-  if (local_window_size == 0 || local_window_size < -1 ||
-      (local_window_size > 0 && mask_kind != FA_MASK_CAUSAL))
+  if (local_window_size == 0 || local_window_size < -1)
     return noalloc_fail(FA_ERR_INVALID_ARG, "bad local_window_size %d", local_window_size);
   if (!std::isfinite(scale)) return noalloc_fail(FA_ERR_INVALID_ARG, "scale must be finite");
   if (scale < 0.f) return noalloc_fail(FA_ERR_UNSUPPORTED, "negative scale");
@@ -131,7 +130,7 @@ extern "C" fa_status_t fa_mha_no_cache_noalloc(void* out, float* lse, const void
   p.Hkv = Hkv;
   p.D = D;
   p.causal = mask_kind == FA_MASK_CAUSAL ? 1 : 0;
-  p.window = local_window_size > 0 ? local_window_size : 0;
+  p.window = local_window_size > 0 && local_window_size < S ? local_window_size : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.lse = lse;

@@ -46,7 +46,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def visible_pairs(S: int, causal: bool, window: int) -> int:
     """Number of (query, key) pairs the mask leaves visible in one (b, h)."""
     if not causal:
-        return S * S
+        if window is None or window <= 0 or window >= S:
+            return S * S
+        W = window  # keys within W - 1 on either side, clipped at both ends
+        return S * (2 * W - 1) - W * (W - 1)
     if window is None or window <= 0 or window >= S:
         return S * (S + 1) // 2
     W = window
@@ -54,8 +57,9 @@ def visible_pairs(S: int, causal: bool, window: int) -> int:
 
 
 def visible_keys_of_row(i: int, S: int, causal: bool, window: int) -> int:
-    hi = i if causal else S - 1
-    lo = max(0, i - window + 1) if (causal and window and window > 0) else 0
+    windowed = window is not None and window > 0
+    hi = i if causal else (min(S - 1, i + window - 1) if windowed else S - 1)
+    lo = max(0, i - window + 1) if windowed else 0
     return hi - lo + 1
 
 

@@ -12,8 +12,9 @@
  * folded into the kernel's addressing), grouped-query attention when k/v
  * carry Hkv < H heads (BShD; query head h reads KV head hk = h / (H / Hkv),
  * i.e. consecutive query heads share a KV head), and a mask that is none,
- * causal (key j visible to query i iff j <= i), or causal with a sliding
- * window of W keys (visible iff j <= i and i - j < W). The S x S score matrix
+ * causal (key j visible to query i iff j <= i), causal with a sliding window
+ * of W keys (visible iff j <= i and i - j < W), or a two-sided window without
+ * the causal mask (visible iff |i - j| < W). The S x S score matrix
  * is never materialised: the bf16 path is a FlashAttention-2 style kernel
  * (online softmax over KV tiles, one final division by the running sum) on
  * the sm_103a tensor cores.
@@ -59,8 +60,9 @@ typedef enum {
  *   scale : multiplies q.k before masking and softmax (the page's `scale`);
  *           finite and >= 0.
  *   mask_kind : FA_MASK_NONE or FA_MASK_CAUSAL.
- *   local_window_size : -1 for no window, else W >= 1 (only with
- *           FA_MASK_CAUSAL): query i sees keys i-W+1 .. i.
+ *   local_window_size : -1 for no window, else W >= 1: with FA_MASK_CAUSAL
+ *           query i sees keys i-W+1 .. i, with FA_MASK_NONE keys i-W+1 ..
+ *           i+W-1 (W >= S hides nothing).
  *   dtype : FA_DTYPE_BF16 or FA_DTYPE_F32.
  *   stream: cudaStream_t (as void*) the work is enqueued on.
  *

@@ -66,7 +66,6 @@ def _call(lib, out=P, lse=None, q=P, k=P, v=P, B=1, S=8, H=2, Hkv=2, D=64, scale
     (dict(mask=2), fa.FA_ERR_INVALID_ARG),
     (dict(window=0), fa.FA_ERR_INVALID_ARG),
     (dict(window=-2), fa.FA_ERR_INVALID_ARG),
-    (dict(mask=0, window=4), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=-1.0), fa.FA_ERR_UNSUPPORTED),

@@ -133,6 +133,12 @@ EDGE_SHAPES = [
     (640, 4, 4, 128, True, 640),
     (700, 2, 1, 128, True, 300),
     (1000, 2, 2, 64, True, -1),
+    # two-sided windows (no causal mask)
+    (129, 2, 1, 128, False, 1),
+    (300, 2, 2, 128, False, 50),
+    (513, 4, 2, 64, False, 129),
+    (700, 2, 2, 128, False, 256),
+    (1000, 2, 1, 64, False, 300),
 ]
 
 
@@ -181,6 +187,17 @@ def test_ragged_long_window_sampled_rows(oracle_mod):
     rows = _sample_rows(S, 31)
     ref_out, ref_lse = oracle_mod.mha_forward(q[:, rows], k, v, scale, True, W, rows=rows)
     _compare(out[:, rows], lse[:, :, rows], ref_out, ref_lse, torch.bfloat16, "S5000 W1000")
+    assert np.isfinite(out).all()
+
+
+def test_two_sided_window_long_sampled_rows(oracle_mod):
+    B, S, H, Hkv, D, W = 1, 6000, 8, 2, 128, 1000
+    q, k, v = make_qkv(B, S, H, Hkv, D, torch.bfloat16, seed=33)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = _run_gpu(q, k, v, scale, False, W)
+    rows = _sample_rows(S, 33)
+    ref_out, ref_lse = oracle_mod.mha_forward(q[:, rows], k, v, scale, False, W, rows=rows)
+    _compare(out[:, rows], lse[:, :, rows], ref_out, ref_lse, torch.bfloat16, "S6000 two-sided W1000")
     assert np.isfinite(out).all()
 
 

@@ -18,12 +18,15 @@ def _brute_pairs(S, causal, window):
         vis &= j <= i
     if window > 0:
         vis &= (i - j) < window
+        if not causal:
+            vis &= (j - i) < window
     return int(vis.sum()), vis.sum(axis=1)
 
 
 @pytest.mark.parametrize("S,causal,window", [(1, False, -1), (7, True, -1), (9, True, 1),
                                              (33, True, 5), (40, True, 40), (41, True, 60),
-                                             (17, False, -1)])
+                                             (17, False, -1), (17, False, 1), (33, False, 5),
+                                             (20, False, 20), (20, False, 19), (7, False, 100)])
 def test_visible_pair_count_matches_brute_force(S, causal, window):
     total, per_row = _brute_pairs(S, causal, window)
     assert bench.visible_pairs(S, causal, window) == total
