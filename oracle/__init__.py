@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the no-cache multi-head attention forward.
+"""fp64 CPU oracle for the multi-head attention forward, without KV cache
+(``mha_forward``) and with one (``mha_forward_kvcache``).
 
 TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's
 CPU-baseline / reference leg may import this package; the product path never
@@ -14,6 +15,9 @@ permutation, rows summing to one), hand-derived fixtures in ``tests/golden/``,
 an independent blockwise online-softmax recomputation (the FlashAttention-2
 loop of the tiny_flash_attn.py page and the normalise-every-step loop of the
 Modular recipe's kernel listing), and torch's fp64 scaled_dot_product_attention.
+``tests/test_oracle_kvcache_pins.py`` pins the KV-cache form the same way
+(torch SDPA on the sliced cache with an explicit end-aligned mask, closed-form
+window means, never reading past the cache length, split-KV recombination).
 """
 from __future__ import annotations
 
@@ -62,6 +66,13 @@ def load_library(path: str):
         ctypes.c_double, ctypes.c_int, ctypes.c_long, ctypes.c_int,
         lp, ctypes.c_long, ctypes.c_int,
     ]
+    if hasattr(lib, "fa_oracle_forward_kvcache"):
+        lib.fa_oracle_forward_kvcache.restype = ctypes.c_int
+        lib.fa_oracle_forward_kvcache.argtypes = [
+            dp, dp, dp, dp, dp,
+            ctypes.c_long, ctypes.c_long, ctypes.c_long, lp, ctypes.c_long, ctypes.c_long,
+            ctypes.c_long, ctypes.c_double, ctypes.c_int, ctypes.c_long, ctypes.c_int,
+        ]
     return lib
 
 
@@ -119,4 +130,38 @@ def mha_forward(q, k, v, scale: float, causal: bool = False, window: int = -1,
         rows_ptr, nrows, int(nthreads or default_threads()))
     if rc != 0:
         raise ValueError(f"fa_oracle_forward failed with status {rc}")
+    return out, lse
+
+
+def mha_forward_kvcache(q, k_cache, v_cache, scale: float, cache_lens=None,
+                        causal: bool = False, window: int = -1,
+                        nthreads: int | None = None, lib=None):
+    """KV-cache attention forward in fp64: batch b holds cache_lens[b] keys
+    (the first rows of k_cache / v_cache, [B, S_cache, Hkv, D]) and its Sq
+    queries q[b] ([B, Sq, H, D]) are the last Sq tokens of that sequence, so
+    query row r sits at position cache_lens[b] - Sq + r. cache_lens = None
+    means S_cache keys everywhere. A query that sees no key gets out = 0 and
+    lse = -inf. Returns (out [B, Sq, H, D], lse [B, H, Sq]) fp64 arrays.
+    """
+    qd, kd, vd = _as_f64(q), _as_f64(k_cache), _as_f64(v_cache)
+    B, S, Hkv, D = kd.shape
+    Sq, H = qd.shape[1], qd.shape[2]
+    if vd.shape != kd.shape or qd.shape[0] != B or qd.shape[3] != D:
+        raise ValueError(f"shape mismatch q{qd.shape} k{kd.shape} v{vd.shape}")
+    lens_ptr, lens_arr = None, None
+    if cache_lens is not None:
+        lens_arr = np.ascontiguousarray(np.asarray(cache_lens, dtype=np.int64).reshape(-1))
+        if lens_arr.size != B:
+            raise ValueError("cache_lens needs one entry per batch")
+        lens_ptr = lens_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_long))
+    out = np.empty((B, Sq, H, D), dtype=np.float64)
+    lse = np.empty((B, H, Sq), dtype=np.float64)
+    dp = ctypes.POINTER(ctypes.c_double)
+    rc = (lib or _load()).fa_oracle_forward_kvcache(
+        qd.ctypes.data_as(dp), kd.ctypes.data_as(dp), vd.ctypes.data_as(dp),
+        out.ctypes.data_as(dp), lse.ctypes.data_as(dp),
+        B, Sq, S, lens_ptr, H, Hkv, D, float(scale), int(bool(causal)), int(window),
+        int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"fa_oracle_forward_kvcache failed with status {rc}")
     return out, lse

@@ -32,6 +32,16 @@
  * mask the keys within distance W - 1 on either side. window = -1 (or 0)
  * means no window.
  *
+ * KV-cache form (fa_oracle_forward_kvcache): the same operator when the keys
+ * and values of batch b are the first L_b rows of a cache of capacity S and
+ * the Sq queries are the last Sq tokens of that sequence, so query row r sits
+ * at position L_b - Sq + r. The pages name only the no-cache operator; this
+ * is the plainest reading of its cached sibling: every step above is
+ * unchanged, the mask is evaluated at the query's position, and keys at
+ * positions >= L_b do not exist (they are never read). A query that sees no
+ * key at all (possible only here, e.g. a causal row whose position is
+ * negative because L_b < Sq) gets out = 0 and lse = -inf.
+ *
  * Everything is fp64. Inputs are fp64 arrays (bf16 / fp32 values widen to
  * fp64 exactly). The score row of one query is materialised (length S); the
  * S x S matrix is not, which changes nothing in the arithmetic.
@@ -55,6 +65,8 @@ typedef struct {
   int head_map;
   const long *rows;
   long nrows;
+  const long *lens; /* KV-cache form: keys per batch (NULL: S keys) */
+  int from_end;     /* KV-cache form: row r sits at position lens[b] - nrows + r */
   long first, last; /* this worker's half-open range of (b, h, r) items */
   int status;
 } fa_oracle_job;
@@ -85,14 +97,15 @@ static void *fa_oracle_worker(void *arg) {
     const long r = item % job->nrows;
     const long h = (item / job->nrows) % H;
     const long b = item / (job->nrows * H);
-    const long i = job->rows ? job->rows[r] : r;
+    const long L = job->lens ? job->lens[b] : S; /* keys 0 .. L-1 exist */
+    const long i = job->from_end ? L - job->nrows + r : (job->rows ? job->rows[r] : r);
     const long hk = job->head_map == 0 ? h / G : h % Hkv;
 
     const double *qrow = job->q + ((b * job->nrows + r) * H + h) * D;
 
     /* Steps 1-3: scaled scores of the visible keys, and their maximum. */
     double m = -INFINITY;
-    for (long j = 0; j < S; ++j) {
+    for (long j = 0; j < L; ++j) {
       seen[j] = (char)key_visible(i, j, job->causal, job->window);
       if (!seen[j]) continue;
       const double *krow = job->k + ((b * S + j) * Hkv + hk) * D;
@@ -105,7 +118,7 @@ static void *fa_oracle_worker(void *arg) {
     /* Step 4: max-subtracted softmax, then the weighted sum of V rows. */
     double denom = 0.0;
     for (long d = 0; d < D; ++d) acc[d] = 0.0;
-    for (long j = 0; j < S; ++j) {
+    for (long j = 0; j < L; ++j) {
       if (!seen[j]) continue;
       const double e = exp(score[j] - m);
       denom += e;
@@ -113,13 +126,56 @@ static void *fa_oracle_worker(void *arg) {
       for (long d = 0; d < D; ++d) acc[d] += e * vrow[d];
     }
     double *orow = job->out + ((b * job->nrows + r) * H + h) * D;
-    for (long d = 0; d < D; ++d) orow[d] = acc[d] / denom; /* NaN if no key */
-    if (job->lse) job->lse[(b * H + h) * job->nrows + r] = m + log(denom);
+    if (denom > 0.0) {
+      for (long d = 0; d < D; ++d) orow[d] = acc[d] / denom;
+      if (job->lse) job->lse[(b * H + h) * job->nrows + r] = m + log(denom);
+    } else { /* no visible key (KV-cache form only) */
+      for (long d = 0; d < D; ++d) orow[d] = 0.0;
+      if (job->lse) job->lse[(b * H + h) * job->nrows + r] = -INFINITY;
+    }
   }
   free(score);
   free(seen);
   free(acc);
   return NULL;
+}
+
+/* Runs the B * H * nrows row jobs on nthreads threads. */
+static int fa_oracle_run(const fa_oracle_job *tmpl, int nthreads) {
+  const long items = tmpl->B * tmpl->H * tmpl->nrows;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > items) nthreads = (int)items;
+  fa_oracle_job *jobs = (fa_oracle_job *)calloc((size_t)nthreads, sizeof(fa_oracle_job));
+  pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+  char *started = (char *)calloc((size_t)nthreads, 1);
+  if (!jobs || !tids || !started) {
+    free(jobs);
+    free(tids);
+    free(started);
+    return FA_ORACLE_NO_MEM;
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t] = *tmpl;
+    jobs[t].first = items * t / nthreads;
+    jobs[t].last = items * (t + 1) / nthreads;
+    jobs[t].status = FA_ORACLE_OK;
+  }
+  for (int t = 1; t < nthreads; ++t)
+    started[t] = pthread_create(&tids[t], NULL, fa_oracle_worker, &jobs[t]) == 0;
+  fa_oracle_worker(&jobs[0]);
+  int status = jobs[0].status;
+  for (int t = 1; t < nthreads; ++t) {
+    if (started[t]) {
+      pthread_join(tids[t], NULL);
+    } else {
+      fa_oracle_worker(&jobs[t]); /* thread creation failed: run inline */
+    }
+    if (jobs[t].status != FA_ORACLE_OK) status = jobs[t].status;
+  }
+  free(jobs);
+  free(tids);
+  free(started);
+  return status;
 }
 
 /*
@@ -147,55 +203,67 @@ int fa_oracle_forward(const double *q, const double *k, const double *v, double 
   if (rows)
     for (long r = 0; r < nrows; ++r)
       if (rows[r] < 0 || rows[r] >= S) return FA_ORACLE_BAD_ARG;
-  if (nthreads < 1) nthreads = 1;
 
-  const long items = B * H * nrows;
-  if (nthreads > items) nthreads = (int)items;
-  fa_oracle_job *jobs = (fa_oracle_job *)calloc((size_t)nthreads, sizeof(fa_oracle_job));
-  pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
-  char *started = (char *)calloc((size_t)nthreads, 1);
-  if (!jobs || !tids || !started) {
-    free(jobs);
-    free(tids);
-    free(started);
-    return FA_ORACLE_NO_MEM;
-  }
-  for (int t = 0; t < nthreads; ++t) {
-    fa_oracle_job *j = &jobs[t];
-    j->q = q;
-    j->k = k;
-    j->v = v;
-    j->out = out;
-    j->lse = lse;
-    j->B = B;
-    j->S = S;
-    j->H = H;
-    j->Hkv = Hkv;
-    j->D = D;
-    j->scale = scale;
-    j->causal = causal;
-    j->window = window;
-    j->head_map = head_map;
-    j->rows = rows;
-    j->nrows = nrows;
-    j->first = items * t / nthreads;
-    j->last = items * (t + 1) / nthreads;
-    j->status = FA_ORACLE_OK;
-  }
-  for (int t = 1; t < nthreads; ++t)
-    started[t] = pthread_create(&tids[t], NULL, fa_oracle_worker, &jobs[t]) == 0;
-  fa_oracle_worker(&jobs[0]);
-  int status = jobs[0].status;
-  for (int t = 1; t < nthreads; ++t) {
-    if (started[t]) {
-      pthread_join(tids[t], NULL);
-    } else {
-      fa_oracle_worker(&jobs[t]); /* thread creation failed: run inline */
-    }
-    if (jobs[t].status != FA_ORACLE_OK) status = jobs[t].status;
-  }
-  free(jobs);
-  free(tids);
-  free(started);
-  return status;
+  fa_oracle_job job;
+  memset(&job, 0, sizeof(job));
+  job.q = q;
+  job.k = k;
+  job.v = v;
+  job.out = out;
+  job.lse = lse;
+  job.B = B;
+  job.S = S;
+  job.H = H;
+  job.Hkv = Hkv;
+  job.D = D;
+  job.scale = scale;
+  job.causal = causal;
+  job.window = window;
+  job.head_map = head_map;
+  job.rows = rows;
+  job.nrows = nrows;
+  return fa_oracle_run(&job, nthreads);
+}
+
+/*
+ * fa_oracle_forward_kvcache -- the KV-cache form (see the header).
+ *   q     : [B, Sq, H, D] fp64, the last Sq tokens of each sequence.
+ *   k, v  : [B, S, Hkv, D] fp64 caches of capacity S; rows >= lens[b] are
+ *           never read.
+ *   lens  : B key counts in [0, S], or NULL for S keys in every batch.
+ *   out   : [B, Sq, H, D] fp64, written; lse: [B, H, Sq] fp64 or NULL.
+ *   Other arguments as fa_oracle_forward (grouped head map).
+ * Returns 0 on success, 1 on a bad argument, 2 when memory runs out.
+ */
+int fa_oracle_forward_kvcache(const double *q, const double *k, const double *v, double *out,
+                              double *lse, long B, long Sq, long S, const long *lens, long H,
+                              long Hkv, long D, double scale, int causal, long window,
+                              int nthreads) {
+  if (!q || !k || !v || !out) return FA_ORACLE_BAD_ARG;
+  if (B < 1 || Sq < 1 || S < 1 || H < 1 || Hkv < 1 || D < 1 || H % Hkv != 0)
+    return FA_ORACLE_BAD_ARG;
+  if (lens)
+    for (long b = 0; b < B; ++b)
+      if (lens[b] < 0 || lens[b] > S) return FA_ORACLE_BAD_ARG;
+
+  fa_oracle_job job;
+  memset(&job, 0, sizeof(job));
+  job.q = q;
+  job.k = k;
+  job.v = v;
+  job.out = out;
+  job.lse = lse;
+  job.B = B;
+  job.S = S;
+  job.H = H;
+  job.Hkv = Hkv;
+  job.D = D;
+  job.scale = scale;
+  job.causal = causal;
+  job.window = window;
+  job.head_map = 0;
+  job.nrows = Sq;
+  job.lens = lens;
+  job.from_end = 1;
+  return fa_oracle_run(&job, nthreads);
 }

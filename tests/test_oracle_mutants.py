@@ -37,8 +37,19 @@ MUTANTS = {
 }
 
 
+# Mistakes specific to the KV-cache form (lengths, end alignment, empty rows).
+KVCACHE_MUTANTS = {
+    "cache_ignores_lengths": ("const long L = job->lens ? job->lens[b] : S;", "const long L = S;"),
+    "cache_position_one_late": ("L - job->nrows + r :", "L - job->nrows + r + 1 :"),
+    "cache_position_from_start": ("job->from_end ? L - job->nrows + r :", "job->from_end ? r :"),
+    "cache_sum_reads_to_capacity": ("for (long j = 0; j < L; ++j) {\n      if (!seen[j]) continue;",
+                                    "for (long j = 0; j < S; ++j) {\n      if (!seen[j]) continue;"),
+    "cache_empty_row_divides_by_zero": ("if (denom > 0.0) {", "if (1) {"),
+}
+
+
 def _build_mutant(name, tmp_path):
-    before, after = MUTANTS[name]
+    before, after = {**MUTANTS, **KVCACHE_MUTANTS}[name]
     src = open(SRC).read()
     assert src.count(before) == 1, f"mutation site for {name} not unique"
     mpath = tmp_path / f"{name}.c"
@@ -90,3 +101,44 @@ def test_planted_mistake_is_caught(oracle_mod, tmp_path, name):
     lib = oracle_mod.load_library(_build_mutant(name, tmp_path))
     with np.errstate(all="ignore"):
         assert _pins_fail(oracle_mod, lib), f"mutant {name} passed every pin"
+
+
+def _kvcache_pins_fail(oracle_mod, lib):
+    """Run a compact set of the KV-cache pins against a (mutant) library."""
+    import test_oracle_kvcache_pins as kv
+
+    def run(fn):
+        try:
+            fn()
+            return False
+        except (AssertionError, ValueError, FloatingPointError):
+            return True
+
+    class Bound:
+        @staticmethod
+        def mha_forward(*a, **kw):
+            return oracle_mod.mha_forward(*a, lib=lib, **kw)
+
+        @staticmethod
+        def mha_forward_kvcache(*a, **kw):
+            return oracle_mod.mha_forward_kvcache(*a, lib=lib, **kw)
+
+    checks = [
+        lambda: kv.test_matches_torch_sdpa_on_sliced_cache(Bound, True, -1, 3),
+        lambda: kv.test_matches_torch_sdpa_on_sliced_cache(Bound, False, 2, 3),
+        lambda: kv.test_identical_keys_average_visible_values(Bound, True, 4),
+        lambda: kv.test_never_reads_past_the_cache_length(Bound, True, -1),
+        lambda: kv.test_queries_before_the_sequence_start_see_nothing(Bound),
+    ]
+    return any(run(c) for c in checks)
+
+
+def test_real_oracle_passes_compact_kvcache_pins(oracle_mod):
+    assert not _kvcache_pins_fail(oracle_mod, None)
+
+
+@pytest.mark.parametrize("name", sorted(KVCACHE_MUTANTS))
+def test_planted_kvcache_mistake_is_caught(oracle_mod, tmp_path, name):
+    lib = oracle_mod.load_library(_build_mutant(name, tmp_path))
+    with np.errstate(all="ignore"):
+        assert _kvcache_pins_fail(oracle_mod, lib), f"mutant {name} passed every pin"
