@@ -1,4 +1,5 @@
-"""GB300-native fused multi-head attention forward without KV cache.
+"""GB300-native fused multi-head attention forward, without KV cache
+(:func:`mha_no_cache`) and over a KV cache (:func:`mha_kv_cache`).
 
 Python binding of the C ABI in ``include/fa_mha.h`` (library
 ``_build/libfa_mha.so``, built by :func:`build`). The binding only marshals
@@ -36,7 +37,7 @@ FA_ERR_TIMEOUT = 4
 
 # Every symbol the header declares (checked by the tests).
 EXPORTS = ("fa_mha_no_cache", "fa_mha_no_cache_strided", "fa_mha_no_cache_noalloc",
-           "fa_device_status",
+           "fa_mha_kv_cache", "fa_mha_kv_cache_plan", "fa_device_status",
            "fa_set_wait_timeout_ns", "fa_set_stall_probe", "fa_status_string",
            "fa_last_error_message", "fa_version", "fa_shutdown")
 
@@ -70,6 +71,13 @@ def load_library(path: str | None = None):
         lib.fa_mha_no_cache_strided.restype = i
         lib.fa_mha_no_cache_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, lp, lp, lp, lp,
                                                 ctypes.c_float, i, i, i, vp]
+        ull = ctypes.c_ulonglong
+        lib.fa_mha_kv_cache.restype = i
+        lib.fa_mha_kv_cache.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float,
+                                        i, i, i, vp, ull, i, vp]
+        lib.fa_mha_kv_cache_plan.restype = i
+        lib.fa_mha_kv_cache_plan.argtypes = [i, i, i, i, i, i, i, i, i, i,
+                                             ctypes.POINTER(i), ctypes.POINTER(ull)]
         lib.fa_device_status.restype = i
         lib.fa_device_status.argtypes = [i, i]
         lib.fa_set_wait_timeout_ns.restype = ctypes.c_ulonglong
@@ -177,6 +185,87 @@ def mha_no_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float
                 out.data_ptr(), lse_ptr, q.data_ptr(), k.data_ptr(), v.data_ptr(),
                 B, S, H, Hkv, D, sq, sk, sv, so, float(scale), _mask_code(mask), int(window),
                 dtype, st.cuda_stream)
+    _check(rc)
+    return (out, lse) if return_lse else out
+
+
+def kv_cache_plan(B: int, Sq: int, S_cache: int, H: int, Hkv: int, D: int, mask="causal",
+                  window: int = -1, num_splits: int = 0, num_sms: int = 0) -> tuple[int, int]:
+    """(splits, workspace bytes) that :func:`mha_kv_cache` uses for these sizes.
+    ``num_sms`` = 0 plans for the current device; n > 0 for an n-SM device
+    (no CUDA call)."""
+    lib = load_library()
+    splits = ctypes.c_int(0)
+    ws = ctypes.c_ulonglong(0)
+    _check(lib.fa_mha_kv_cache_plan(int(B), int(Sq), int(S_cache), int(H), int(Hkv), int(D),
+                                    _mask_code(mask), int(window), int(num_splits), int(num_sms),
+                                    ctypes.byref(splits), ctypes.byref(ws)))
+    return int(splits.value), int(ws.value)
+
+
+def mha_kv_cache(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 cache_lens: torch.Tensor | None = None, scale: float | None = None,
+                 mask="causal", window: int = -1, *, num_splits: int = 0,
+                 out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                 return_lse: bool = False, workspace: torch.Tensor | None = None,
+                 stream: torch.cuda.Stream | None = None):
+    """Attention over a KV cache (bf16, tensor cores) on the current CUDA device.
+
+    q: [B, Sq, H, D], the last Sq tokens of each sequence; k_cache, v_cache:
+    [B, S_cache, Hkv, D] whose first cache_lens[b] rows hold batch b's keys and
+    values (cache_lens: int32 CUDA tensor [B], or None for full caches). Query
+    row s of batch b sits at position cache_lens[b] - Sq + s; the mask is
+    evaluated there. All tensors contiguous bf16. ``num_splits`` = 0 lets the
+    library pick the key-range split; the workspace it needs is allocated here
+    unless given. Returns out [B, Sq, H, D] (and lse [B, H, Sq] fp32 if
+    ``return_lse``).
+    """
+    if q.dim() != 4 or k_cache.dim() != 4 or v_cache.dim() != 4:
+        raise ValueError("q, k_cache, v_cache must be 4-D (BSHD)")
+    B, Sq, H, D = q.shape
+    if k_cache.shape != v_cache.shape or k_cache.shape[0] != B or k_cache.shape[3] != D:
+        raise ValueError(f"cache shapes {tuple(k_cache.shape)}/{tuple(v_cache.shape)} do not "
+                         f"match q {tuple(q.shape)} (expected [B, S_cache, Hkv, D])")
+    S_cache, Hkv = k_cache.shape[1], k_cache.shape[2]
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bf16")
+        if t.device != q.device:
+            raise ValueError("q and the caches must be on one device")
+    if cache_lens is not None and (cache_lens.dtype != torch.int32 or cache_lens.numel() != B
+                                   or not cache_lens.is_contiguous()
+                                   or cache_lens.device != q.device):
+        raise ValueError("cache_lens must be a contiguous int32 [B] tensor on q's device")
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous() \
+            or out.device != q.device:
+        raise ValueError("out must be a contiguous tensor with q's shape, dtype and device")
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    elif lse is not None and (lse.shape != (B, H, Sq) or lse.dtype != torch.float32
+                              or not lse.is_contiguous() or lse.device != q.device):
+        raise ValueError("lse must be a contiguous fp32 [B, H, Sq] tensor on q's device")
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        _, ws_bytes = kv_cache_plan(B, Sq, S_cache, H, Hkv, D, mask, window, num_splits)
+        if ws_bytes > 0 and (workspace is None or workspace.numel() * workspace.element_size()
+                             < ws_bytes):
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+        st = stream if stream is not None else torch.cuda.current_stream(q.device)
+        rc = lib.fa_mha_kv_cache(
+            out.data_ptr(), lse.data_ptr() if lse is not None else None, q.data_ptr(),
+            k_cache.data_ptr(), v_cache.data_ptr(),
+            cache_lens.data_ptr() if cache_lens is not None else None,
+            B, Sq, S_cache, H, Hkv, D, float(scale), _mask_code(mask), int(window),
+            int(num_splits), workspace.data_ptr() if ws_bytes > 0 else None,
+            int(ws_bytes), DTYPE_BF16, st.cuda_stream)
     _check(rc)
     return (out, lse) if return_lse else out
 

@@ -1,6 +1,7 @@
 // fa_api.cu -- the C ABI declared in include/fa_mha.h: argument validation,
 // per-device state (status word), TMA tensor-map encoding and dispatch to the
-// bf16 tensor-core kernel or the fp32 CUDA-core kernel.
+// bf16 tensor-core kernel or the fp32 CUDA-core kernel, and the KV-cache
+// entry points (work plan: tile geometry, key-range splits, workspace).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -86,7 +87,7 @@ namespace fa {
 void record_error_message(const char* msg) { snprintf(t_message, sizeof(t_message), "%s", msg); }
 
 bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D,
-                            BshdStrides st) {
+                            BshdStrides st, int box_heads, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   st = resolve_strides(st, S, heads, D);
@@ -95,7 +96,9 @@ bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, in
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.h) * 2,
                                  static_cast<cuuint64_t>(st.s) * 2,
                                  static_cast<cuuint64_t>(st.b) * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
+  if (box_heads < 1 || box_heads > 256 || box_rows < 1 || box_rows > 256) return false;
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_heads),
+                             static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -207,9 +210,179 @@ fa_status_t forward(void* out, float* lse, const void* q, const void* k, const v
   return FA_OK;
 }
 
+// ------------------------------------------------------------- KV cache
+
+// How the KV-cache kernel cuts the work (see fa_mha_kv_cache_plan).
+struct KvPlan {
+  int G, Pq, R, n_ptiles;
+  int window;  // effective window (0: none)
+  int splits, tiles_per_split;
+  unsigned long long o_part_bytes, workspace_bytes;
+};
+
+constexpr int kMaxSplits = 128;
+
+unsigned long long align256(unsigned long long x) { return (x + 255ull) & ~255ull; }
+
+// Validates the size, mask and split arguments of the KV-cache entry points.
+fa_status_t check_kv_args(int B, int Sq, int S_cache, int H, int Hkv, int D, int mask_kind,
+                          int local_window_size, int num_splits) {
+  if (B < 1 || Sq < 1 || S_cache < 1 || H < 1 || Hkv < 1)
+    return fail(FA_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d Sq=%d S_cache=%d H=%d Hkv=%d)", B,
+                Sq, S_cache, H, Hkv);
+  if (H % Hkv != 0)
+    return fail(FA_ERR_INVALID_ARG, "H=%d is not a multiple of Hkv=%d", H, Hkv);
+  if (mask_kind != FA_MASK_NONE && mask_kind != FA_MASK_CAUSAL)
+    return fail(FA_ERR_INVALID_ARG, "unknown mask kind %d", mask_kind);
+  if (local_window_size == 0 || local_window_size < -1)
+    return fail(FA_ERR_INVALID_ARG, "local_window_size must be -1 or >= 1 (got %d)",
+                local_window_size);
+  if (num_splits < 0) return fail(FA_ERR_INVALID_ARG, "num_splits must be >= 0");
+  if (D != 64 && D != 128) return fail(FA_ERR_UNSUPPORTED, "head dim D=%d (built: 64, 128)", D);
+  if (H / Hkv > 128)
+    return fail(FA_ERR_UNSUPPORTED, "H / Hkv = %d query heads per KV head (at most 128)", H / Hkv);
+  const long long q_elems = static_cast<long long>(B) * Sq * H * D;
+  const long long c_elems = static_cast<long long>(B) * S_cache * Hkv * D;
+  if (q_elems >= (1ll << 40) || c_elems >= (1ll << 40) ||
+      static_cast<long long>(S_cache) * Hkv * D * 2 >= (1ll << 39))
+    return fail(FA_ERR_UNSUPPORTED, "problem too large");
+  return FA_OK;
+}
+
+KvPlan make_kv_plan(int B, int Sq, int S_cache, int H, int Hkv, int D, int causal,
+                    int local_window_size, int num_splits, int num_sms) {
+  KvPlan k{};
+  k.G = H / Hkv;
+  k.Pq = Sq < 128 / k.G ? Sq : 128 / k.G;
+  k.R = k.G * k.Pq;
+  k.n_ptiles = (Sq + k.Pq - 1) / k.Pq;
+  // A window reaching past every key of the cache hides nothing.
+  k.window = local_window_size > 0 && local_window_size < S_cache ? local_window_size : 0;
+  // Most KV tiles one position tile can need.
+  const long long all_tiles = (S_cache + 127) / 128;
+  long long max_tiles = all_tiles;
+  if (k.window > 0) {
+    const long long span = causal ? (k.Pq - 1ll + k.window) : (k.Pq + 2ll * k.window - 2);
+    max_tiles = (span + 127) / 128 + 1;
+    if (max_tiles > all_tiles) max_tiles = all_tiles;
+  }
+  long long splits = num_splits;
+  if (splits == 0) {
+    // Auto: enough CTAs (one per SM at most) to fill the GPU once.
+    const long long units = static_cast<long long>(B) * Hkv * k.n_ptiles;
+    splits = (num_sms + units / 2) / units;
+    if (splits < 1) splits = 1;
+  }
+  if (splits > kMaxSplits) splits = kMaxSplits;
+  if (splits > max_tiles) splits = max_tiles;
+  k.tiles_per_split = static_cast<int>((max_tiles + splits - 1) / splits);
+  k.splits = static_cast<int>((max_tiles + k.tiles_per_split - 1) / k.tiles_per_split);
+  if (k.splits > 1) {
+    const unsigned long long rows = static_cast<unsigned long long>(B) * Sq * H;
+    k.o_part_bytes = align256(k.splits * rows * D * 4ull);
+    k.workspace_bytes = k.o_part_bytes + align256(k.splits * rows * 4ull);
+  }
+  return k;
+}
+
+fa_status_t current_sm_count(int* out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  err = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaDeviceGetAttribute(SM count)");
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+fa_status_t fa_mha_kv_cache_plan(int B, int Sq, int S_cache, int H, int Hkv, int D, int mask_kind,
+                                 int local_window_size, int num_splits, int num_sms,
+                                 int* splits_out, unsigned long long* workspace_bytes_out) {
+  if (splits_out == nullptr || workspace_bytes_out == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "null output pointer");
+  fa_status_t st = check_kv_args(B, Sq, S_cache, H, Hkv, D, mask_kind, local_window_size,
+                                 num_splits);
+  if (st != FA_OK) return st;
+  if (num_sms < 0) return fail(FA_ERR_INVALID_ARG, "num_sms must be >= 0");
+  if (num_sms == 0 && (st = current_sm_count(&num_sms)) != FA_OK) return st;
+  const KvPlan k = make_kv_plan(B, Sq, S_cache, H, Hkv, D, mask_kind == FA_MASK_CAUSAL,
+                                local_window_size, num_splits, num_sms);
+  *splits_out = k.splits;
+  *workspace_bytes_out = k.workspace_bytes;
+  return FA_OK;
+}
+
+fa_status_t fa_mha_kv_cache(void* out, float* lse, const void* q, const void* k_cache,
+                            const void* v_cache, const int* cache_lens, int B, int Sq,
+                            int S_cache, int H, int Hkv, int D, float scale, int mask_kind,
+                            int local_window_size, int num_splits, void* workspace,
+                            unsigned long long workspace_bytes, int dtype, void* stream) {
+  if (out == nullptr || q == nullptr || k_cache == nullptr || v_cache == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  fa_status_t st = check_kv_args(B, Sq, S_cache, H, Hkv, D, mask_kind, local_window_size,
+                                 num_splits);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+  if (scale < 0.f) return fail(FA_ERR_UNSUPPORTED, "negative scale is not supported");
+  if (dtype != FA_DTYPE_BF16)
+    return fail(FA_ERR_UNSUPPORTED, "the KV-cache entry point takes bf16 only (dtype %d)", dtype);
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      (lse != nullptr && !aligned(lse, 4)) || (cache_lens != nullptr && !aligned(cache_lens, 4)) ||
+      (workspace != nullptr && !aligned(workspace, 16)))
+    return fail(FA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned (lse, cache_lens: 4)");
+
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(FA_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+  if ((st = current_sm_count(&sms)) != FA_OK) return st;
+  const KvPlan plan = make_kv_plan(B, Sq, S_cache, H, Hkv, D, mask_kind == FA_MASK_CAUSAL,
+                                   local_window_size, num_splits, sms);
+  if (plan.workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < plan.workspace_bytes))
+    return fail(FA_ERR_INVALID_ARG, "workspace of %llu bytes needed (%d splits), %llu given",
+                plan.workspace_bytes, plan.splits, workspace != nullptr ? workspace_bytes : 0ull);
+  if (static_cast<long long>(plan.splits) * Hkv * plan.n_ptiles * B > 0x7fffffffll)
+    return fail(FA_ERR_UNSUPPORTED, "problem too large (grid)");
+  unsigned* status = nullptr;
+  if ((st = device_status_word(dev, &status)) != FA_OK) return st;
+
+  fa::DecodeProblem p{};
+  p.B = B;
+  p.Sq = Sq;
+  p.Scache = S_cache;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.G = plan.G;
+  p.Pq = plan.Pq;
+  p.R = plan.R;
+  p.n_ptiles = plan.n_ptiles;
+  p.causal = mask_kind == FA_MASK_CAUSAL ? 1 : 0;
+  p.window = plan.window;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.lens = cache_lens;
+  p.splits = plan.splits;
+  p.tiles_per_split = plan.tiles_per_split;
+  p.lse = lse;
+  if (plan.splits > 1) {
+    p.o_part = static_cast<float*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.o_part_bytes);
+  }
+  p.status = status;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.stall_probe = g_stall_probe.load();
+  err = fa::launch_decode_bf16_tc(p, out, q, k_cache, v_cache, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "KV-cache kernel launch");
+  return FA_OK;
+}
 
 fa_status_t fa_mha_no_cache(void* out, float* lse, const void* q, const void* k, const void* v,
                             int B, int S, int H, int Hkv, int D, float scale, int mask_kind,

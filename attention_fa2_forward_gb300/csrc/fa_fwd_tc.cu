@@ -39,13 +39,14 @@
 #include <cmath>
 
 #include "fa_internal.h"
+#include "fa_tile.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
 namespace {
 
 constexpr int kBM = 128;                          // query rows per Q tile (= TMEM lanes)
-constexpr int kBN = 128;                          // keys per K/V tile
+constexpr int kBN = tile::kBN;                    // keys per K/V tile
 constexpr int kQTiles = 2;                        // Q tiles per CTA
 constexpr int kSoftmaxWarps = 4 * kQTiles;        // one warpgroup per Q tile
 constexpr int kMmaWarp = kSoftmaxWarps;           // warp 8
@@ -72,35 +73,6 @@ struct Cfg {
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColO = 256;                   // O_t at kColO + t * D
 };
-
-// Pairs of score columns whose exponential runs on the FMA pipe (a degree-3
-// polynomial) instead of the MUFU unit: kPolyPer8 of every 8 pairs, spread
-// evenly. The MUFU unit (16 exp2 per clock per SM) is as busy as the tensor
-// core without this; the split balances MUFU and FMA-pipe issue.
-constexpr int kPolyPer8 = 0;
-__host__ __device__ constexpr bool poly_pair(int i) {
-  return ((i & 7) * kPolyPer8) / 8 != (((i & 7) + 1) * kPolyPer8) / 8;
-}
-
-constexpr uint32_t kNegInfBits = 0xff800000u;
-
-// Hides (-inf) the scores outside the visible key columns [vlo, vhi] of the
-// tile; with a zero scale the visible ones become 0 (the caller then uses 1
-// as the multiplier, which keeps -inf * 0 out of the hidden lanes).
-// Branch-free: one unsigned range test and two selects per element.
-__device__ __forceinline__ void mask_tile(uint32_t* r, int vlo, int vhi, bool zero_scale) {
-  int lo = max(vlo, 0);
-  const int hi = min(vhi, kBN - 1);
-  unsigned span = static_cast<unsigned>(hi - lo);
-  if (hi < lo) {  // nothing visible in this tile
-    lo = 2 * kBN;
-    span = 0;
-  }
-  const uint32_t keep = zero_scale ? 0u : 0xffffffffu;
-#pragma unroll
-  for (int e = 0; e < kBN; ++e)
-    r[e] = static_cast<unsigned>(e - lo) <= span ? (r[e] & keep) : kNegInfBits;
-}
 
 // Visibility bounds of query row i (keys lo..hi inclusive may be visible).
 struct RowBounds {
@@ -410,18 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // Tiles that straddle the mask boundary (or a zero scale): hide the
       // invisible scores in place, then every tile takes the same path.
-      if (!full || zero_scale) mask_tile(r, vlo, vhi, zero_scale);
+      if (!full || zero_scale) tile::mask_cols(r, vlo, vhi, zero_scale);
 
       // Row maximum of the (visible) scores.
-      float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < kBN; e += 8) {
-        a0 = ptx::max3(a0, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-        a1 = ptx::max3(a1, __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-        a2 = ptx::max3(a2, __uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
-        a3 = ptx::max3(a3, __uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
-      }
-      const float mx = ptx::max3(a0, a1, fmaxf(a2, a3));
+      const float mx = tile::row_max(r);
       const float m_tile = mx == -INFINITY ? -INFINITY : mx * ce;
       const float m_new = fmaxf(m_use, m_tile);
       const bool first = j == tlo;
@@ -436,35 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float neg_base = m_use == -INFINITY ? 0.f : -m_use;
 
-      // P = 2^(x - m_use) (hidden scores are -inf and give 0), row sum, and
-      // bf16 pairs written over S. Pairs of columns: x = s * c - m with packed
-      // FMAs; kPolyPer8 of every 8 pairs take 2^x on the FMA pipe.
-      float row_sum;
-      {
-        const uint64_t c2 = ptx::pair(__float_as_uint(ce), __float_as_uint(ce));
-        const uint64_t nb2 = ptx::pair(__float_as_uint(neg_base), __float_as_uint(neg_base));
-        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
-#pragma unroll
-        for (int i = 0; i < kBN / 2; ++i) {
-          uint32_t lo, hi;
-          ptx::unpair(ptx::fma2(ptx::pair(r[2 * i], r[2 * i + 1]), c2, nb2), lo, hi);
-          if (poly_pair(i)) {
-            ptx::exp2_poly3_pair(lo, hi);
-          } else {
-            lo = __float_as_uint(ptx::ex2_approx(__uint_as_float(lo)));
-            hi = __float_as_uint(ptx::ex2_approx(__uint_as_float(hi)));
-          }
-          const uint64_t pp = ptx::pair(lo, hi);
-          if ((i & 3) == 0) acc0 = ptx::add2(acc0, pp);
-          if ((i & 3) == 1) acc1 = ptx::add2(acc1, pp);
-          if ((i & 3) == 2) acc2 = ptx::add2(acc2, pp);
-          if ((i & 3) == 3) acc3 = ptx::add2(acc3, pp);
-          r[i] = ptx::pack_bf16x2(__uint_as_float(lo), __uint_as_float(hi));
-        }
-        uint32_t u0, u1;
-        ptx::unpair(ptx::add2(ptx::add2(acc0, acc1), ptx::add2(acc2, acc3)), u0, u1);
-        row_sum = __uint_as_float(u0) + __uint_as_float(u1);
-      }
+      // P = 2^(x - m_use) (hidden scores are -inf and give 0) as bf16 pairs
+      // written over S, and the row sum.
+      const float row_sum = tile::exp2_to_bf16(r, ce, neg_base);
       l_run = l_run * alpha + row_sum;
 #pragma unroll
       for (int c0 = 0; c0 < kBN / 2; c0 += 32) ptx::tmem_st_32x32b_x32(tS + c0, r + c0);
@@ -510,22 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld_32x32b_x32(tO + c0, o);
         ptx::tmem_wait_ld();
         ptx::reg_fence<32>(o);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint4 pk;
-          pk.x = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l,
-                                  __uint_as_float(o[8 * u + 1]) * inv_l);
-          pk.y = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l,
-                                  __uint_as_float(o[8 * u + 3]) * inv_l);
-          pk.z = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l,
-                                  __uint_as_float(o[8 * u + 5]) * inv_l);
-          pk.w = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l,
-                                  __uint_as_float(o[8 * u + 7]) * inv_l);
-          const int chunk = ((c0 & 63) >> 3) + u;  // 16-byte chunk within the 128-byte row
-          const int box = c0 >> 6;
-          const int phys = chunk ^ (row & 7);       // 128-byte swizzle
-          *reinterpret_cast<uint4*>(stage + box * kBoxBytes + row * 128 + phys * 16) = pk;
-        }
+        tile::stage_bf16_sw128(stage, kBoxBytes, row, c0, o, inv_l);
       }
       ptx::fence_proxy_async_smem();
     }

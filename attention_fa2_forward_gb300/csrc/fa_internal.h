@@ -42,6 +42,30 @@ struct FwdProblem {
   BshdStrides sq, sk, sv, so;  // layouts of q, k, v, out (zero: dense)
 };
 
+// Attention over a KV cache (bf16, tensor cores): batch b holds L_b keys at
+// the start of a [B, Scache, Hkv, D] cache; its Sq queries ([B, Sq, H, D])
+// sit at positions L_b - Sq .. L_b - 1. A Q tile packs Pq positions x G heads
+// of one KV head (R = G * Pq <= 128 rows); each (b, KV head, position tile)
+// is cut into `splits` ranges of `tiles_per_split` KV tiles.
+struct DecodeProblem {
+  int B, Sq, Scache, H, Hkv, D;
+  int G, Pq, R, n_ptiles;  // tile geometry
+  int causal, window;      // mask, evaluated at the query's position
+  float scale, scale_log2;
+  const int* lens;         // [B] keys per batch (clamped to [0, Scache]) or nullptr: Scache
+  int splits, tiles_per_split;
+  float* lse;              // [B, H, Sq] fp32 or nullptr
+  float* o_part;           // [splits, B, Sq, H, D] fp32 partial O / l (splits > 1)
+  float* lse_part;         // [splits, B, H, Sq] fp32 partial LSE (splits > 1)
+  unsigned* status;
+  unsigned long long wait_limit_ns;
+  int stall_probe;
+};
+
+// Launches the KV-cache kernel (and, with splits > 1, the combine kernel).
+cudaError_t launch_decode_bf16_tc(const DecodeProblem& p, void* out, const void* q, const void* k,
+                                  const void* v, cudaStream_t stream);
+
 // Tensor-core (tcgen05) bf16 forward. q/k/v/out are device pointers to
 // 16-byte-aligned dense BSHD / BShD bf16 tensors. Returns a cudaError_t.
 cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, const void* k,
@@ -55,9 +79,9 @@ cudaError_t launch_fwd_f32_simt(const FwdProblem& p, float* out, const float* q,
 void record_error_message(const char* msg);
 
 // Encodes a 4-D BSHD tensor map (dims D, heads, S, B; element strides `st`,
-// D contiguous) for bf16 data with a {64, 1, 128, 1} box and 128-byte
-// swizzle. Returns false on failure.
+// D contiguous) for bf16 data with a {64, box_heads, box_rows, 1} box and
+// 128-byte swizzle. Returns false on failure.
 bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D,
-                            BshdStrides st);
+                            BshdStrides st, int box_heads = 1, int box_rows = 128);
 
 }  // namespace fa

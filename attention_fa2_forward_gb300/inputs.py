@@ -83,3 +83,71 @@ def workload_inputs(w: Workload, S: int | None = None, B: int | None = None):
     """Inputs of a workload (optionally with a different S or B, same recipe)."""
     return make_qkv(B or w.B, S or w.S, w.H, w.Hkv, w.D, w.torch_dtype, w.seed,
                     q_std=w.q_std, k_std=w.k_std, v_dist=w.v_dist)
+
+
+# ---------------------------------------------------------------- KV cache
+
+@dataclass(frozen=True)
+class KvWorkload:
+    """One attention step over a KV cache: B sequences whose keys and values
+    fill the first lens[b] rows of [B, S_cache, Hkv, D] caches, with Sq new
+    query tokens each (Sq = 1: one decoding step)."""
+    name: str
+    B: int
+    Sq: int
+    S_cache: int
+    H: int
+    Hkv: int
+    D: int
+    causal: bool = True
+    window: int = -1
+    ragged: bool = False  # lens drawn uniformly from [Sq, S_cache]; else all S_cache
+    seed: int = 2000
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / (self.D ** 0.5)
+
+    def describe(self) -> str:
+        mask = "causal" if self.causal else "none"
+        if self.window > 0:
+            mask += f"+window{self.window}"
+        lens = "ragged" if self.ragged else "full"
+        return (f"B{self.B} Sq{self.Sq} S_cache{self.S_cache} ({lens}) H{self.H} "
+                f"Hkv{self.Hkv} D{self.D} bf16 {mask}")
+
+
+# Decoding steps: many short sequences, one long sequence (the key range is
+# cut into splits), and a ragged batch of 4-token (speculative) steps.
+KV_WORKLOADS = {
+    "decode_b16_l8192_gqa_d128": KvWorkload("decode_b16_l8192_gqa_d128", 16, 1, 8192, 32, 8,
+                                            128, seed=2001),
+    "decode_b1_l131072_gqa_d128": KvWorkload("decode_b1_l131072_gqa_d128", 1, 1, 131072, 32, 8,
+                                             128, seed=2002),
+    "decode_b8_l32768_sq4_ragged": KvWorkload("decode_b8_l32768_sq4_ragged", 8, 4, 32768, 32, 8,
+                                              128, ragged=True, seed=2003),
+}
+
+
+def make_kv_cache(B: int, Sq: int, S_cache: int, H: int, Hkv: int, D: int, seed: int,
+                  ragged: bool = False, lens=None):
+    """CPU bf16 tensors q [B, Sq, H, D], k_cache and v_cache [B, S_cache, Hkv, D]
+    (every row random, including rows past the lengths) and the int32 lengths
+    [B]: ``lens`` if given, else drawn uniformly from [Sq, S_cache] when
+    ``ragged``, else S_cache."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((B, Sq, H, D), generator=g, dtype=torch.float32)
+    k = torch.randn((B, S_cache, Hkv, D), generator=g, dtype=torch.float32)
+    v = torch.randn((B, S_cache, Hkv, D), generator=g, dtype=torch.float32)
+    if lens is None:
+        if ragged:
+            lens = torch.randint(min(Sq, S_cache), S_cache + 1, (B,), generator=g)
+        else:
+            lens = torch.full((B,), S_cache)
+    lens = torch.as_tensor(lens, dtype=torch.int32).reshape(B)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16), lens
+
+
+def kv_workload_inputs(w: KvWorkload):
+    return make_kv_cache(w.B, w.Sq, w.S_cache, w.H, w.Hkv, w.D, w.seed, ragged=w.ragged)

@@ -74,6 +74,41 @@ def algorithmic_bytes(w) -> int:
             + 4 * w.B * w.H * w.S)
 
 
+# ----------------------------------------------------------------- KV-cache accounting
+KV_METRIC = "KV-cache attention HBM GB/s (algorithmic bytes: visible cache rows, Q, O, LSE)"
+KV_KERNEL_NAME = "fa_decode_bf16_tc_kernel"
+
+
+def kv_row_range(L: int, Sq: int, s: int, causal: bool, window: int):
+    """Visible keys [lo, hi] of query row s of a batch holding L keys."""
+    pos = L - Sq + s
+    windowed = window is not None and window > 0
+    lo = max(0, pos - window + 1) if windowed else 0
+    hi = min(pos, L - 1) if causal else (min(pos + window - 1, L - 1) if windowed else L - 1)
+    return lo, hi
+
+
+def kv_flops(w, lens) -> float:
+    pairs = 0
+    for L in lens:
+        for s in range(w.Sq):
+            lo, hi = kv_row_range(int(L), w.Sq, s, w.causal, w.window)
+            pairs += max(0, hi - lo + 1)
+    return 4.0 * w.H * w.D * pairs
+
+
+def kv_algorithmic_bytes(w, lens) -> int:
+    """Cache rows some query of the batch sees (K and V, once), Q read, O and
+    LSE written."""
+    rows = 0
+    for L in lens:
+        lo, _ = kv_row_range(int(L), w.Sq, 0, w.causal, w.window)
+        _, hi = kv_row_range(int(L), w.Sq, w.Sq - 1, w.causal, w.window)
+        rows += max(0, hi - lo + 1)
+    return (2 * rows * w.Hkv * w.D * 2 + 2 * w.B * w.Sq * w.H * w.D * 2
+            + 4 * w.B * w.H * w.Sq)
+
+
 # ----------------------------------------------------------------- peaks / traffic
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -85,27 +120,44 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_digest() -> str:
+def kernel_source_digest(kernel_file: str = "fa_fwd_tc.cu") -> str:
+    """Digest of a kernel's source file and every local header it includes
+    (transitively): a profile taken on other source no longer applies."""
     csrc = os.path.join(ROOT, "attention_fa2_forward_gb300", "csrc")
+    inc_dirs = [csrc, os.path.join(ROOT, "include")]
+    seen, todo = set(), [kernel_file]
+    while todo:
+        name = todo.pop()
+        if name in seen:
+            continue
+        for d in inc_dirs:
+            path = os.path.join(d, name)
+            if os.path.exists(path):
+                seen.add(name)
+                with open(path) as f:
+                    todo += re.findall(r'^#include "([^"]+)"', f.read(), flags=re.M)
+                break
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.startswith("fa_fwd_tc") or name.endswith((".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(seen):
+        path = next(os.path.join(d, name) for d in inc_dirs
+                    if os.path.exists(os.path.join(d, name)))
+        with open(path, "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, kernel: str = KERNEL_NAME,
+                     kernel_file: str = "fa_fwd_tc.cu"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (matching digest); else None."""
-    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)\s*\(kernel source digest ([0-9a-f]+)\)",
                   text)
-    if not m or m.group(2) != kernel_source_digest():
+    if not m or m.group(2) != kernel_source_digest(kernel_file):
         return None
     return int(m.group(1))
 
@@ -395,6 +447,160 @@ def bench_ours(args, w, world, rank, local, dist):
     }
 
 
+def bench_kv_reference(args, w, world, rank):
+    """The fp64 oracle's KV-cache form on the host cores, on the first batches
+    of the workload (bounded to a few seconds per step)."""
+    if rank != 0:
+        return None
+    import oracle
+    from attention_fa2_forward_gb300.inputs import kv_workload_inputs
+    oracle.build()
+    q, k, v, lens = kv_workload_inputs(w)
+    nthreads = oracle.default_threads()
+    nb = max(1, min(w.B, 2))
+
+    def one():
+        t0 = time.perf_counter()
+        oracle.mha_forward_kvcache(q[:nb], k[:nb], v[:nb], w.scale, lens[:nb].numpy(), w.causal,
+                                   w.window, nthreads=nthreads)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one()
+    times = [one() for _ in range(args.steps)]
+    sub = lens[:nb].tolist()
+    byts = kv_algorithmic_bytes(type(w)(**{**w.__dict__, "B": nb}), sub)
+    value = byts * args.steps / sum(times) / 1e9
+    sample = f"batches 0..{nb - 1} of {w.B} (all heads, all query rows): {byts / 1e6:.1f} MB"
+    return {
+        "impl": "reference", "metric": KV_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sum(times) / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.describe(), "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def bench_kv_ours(args, w, world, rank, local, dist):
+    """One attention step over resident KV caches per timed step (the caches
+    live in HBM, as in decoding; e2e copies the step's queries and lengths in
+    and its output out)."""
+    import torch
+
+    import attention_fa2_forward_gb300 as fa
+    from attention_fa2_forward_gb300.inputs import kv_workload_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    q_h, k_h, v_h, lens_h = kv_workload_inputs(w)
+    q, k, v, lens = q_h.to(dev), k_h.to(dev), v_h.to(dev), lens_h.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    mask = "causal" if w.causal else "none"
+    splits, ws_bytes = fa.kv_cache_plan(w.B, w.Sq, w.S_cache, w.H, w.Hkv, w.D, mask, w.window,
+                                        args.splits)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+    def step():
+        fa.mha_kv_cache(q, k, v, lens, w.scale, mask, w.window, num_splits=args.splits, out=out,
+                        lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if fa.device_status() != fa.FA_OK:
+        raise RuntimeError("kernel reported a timed-out wait during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    for s in range(args.steps):
+        flush.zero_()
+        starts[s].record(stream)
+        step()
+        ends[s].record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    barrier(dist)
+    local_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
+    total_ms = max_over_ranks(local_ms, dist)
+    if fa.device_status() != fa.FA_OK:
+        raise RuntimeError("kernel reported a timed-out wait in the timed region")
+
+    lens_list = lens_h.tolist()
+    byts = kv_algorithmic_bytes(w, lens_list)
+    flops = kv_flops(w, lens_list)
+    ms_per_step = total_ms / args.steps
+    value = world * byts / (ms_per_step * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        qp, lp = q_h.pin_memory(), lens_h.pin_memory()
+        outp = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        e2e_steps = max(1, min(args.steps, 20))
+
+        def e2e_step():
+            q.copy_(qp, non_blocking=True)
+            lens.copy_(lp, non_blocking=True)
+            step()
+            outp.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist) / e2e_steps
+        e2e = {"value": world * byts / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": qp.numel() * qp.element_size() + lp.numel() * 4,
+               "d2h_bytes_per_step": outp.numel() * outp.element_size(),
+               "ms_per_step": e2e_ms, "note": "KV caches resident on the device"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res = bench_kv_reference(argparse.Namespace(steps=1, warmup=0), w, 1, 0)
+        cpu = res["cpu_baseline"]
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = byts / (local_ms / args.steps * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": profiled_traffic(w.name, KV_KERNEL_NAME, "fa_decode_tc.cu"),
+                "peak_source": f"{peak_src} (HBM copy, MEASURED_PEAKS.json)"
+                if peak_src == "measured" else "fallback",
+                "algorithmic_bytes": byts,
+                "tflops": flops / (local_ms / args.steps * 1e-3) / 1e12}
+    return {
+        "metric": KV_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.describe(), "B": w.B, "Sq": w.Sq,
+                   "S_cache": w.S_cache, "H": w.H, "Hkv": w.Hkv, "D": w.D, "mask": mask,
+                   "window": w.window, "lens": "ragged" if w.ragged else "full",
+                   "splits": splits, "bytes_per_step": byts, "flops_per_step": flops,
+                   "l2": "flushed (256 MiB write) before every step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": clocks.summary(), "gpu_launches": args.steps * (2 if splits > 1 else 1),
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -405,20 +611,26 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--splits", type=int, default=0,
+                    help="KV-cache workloads: key-range splits (0: the library's choice)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    from attention_fa2_forward_gb300.inputs import WORKLOADS
-    w = WORKLOADS[args.workload]
+    from attention_fa2_forward_gb300.inputs import KV_WORKLOADS, WORKLOADS
+    kv = args.workload in KV_WORKLOADS
+    if not kv and args.workload not in WORKLOADS:
+        ap.error(f"unknown workload {args.workload!r} "
+                 f"(choose from {sorted(WORKLOADS) + sorted(KV_WORKLOADS)})")
+    w = KV_WORKLOADS[args.workload] if kv else WORKLOADS[args.workload]
     world, rank, local = dist_env()
     if args.impl == "reference":
-        res = bench_reference(args, w, world, rank)
+        res = (bench_kv_reference if kv else bench_reference)(args, w, world, rank)
         if res is not None:
             print(json.dumps(res), flush=True)
         return 0
     dist = init_dist(world, "nccl")
-    res = bench_ours(args, w, world, rank, local, dist)
+    res = (bench_kv_ours if kv else bench_ours)(args, w, world, rank, local, dist)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if dist is not None:

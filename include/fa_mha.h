@@ -1,6 +1,6 @@
 /*
- * fa_mha.h -- C ABI of the GB300 (sm_103a) fused multi-head attention forward
- * without KV cache.
+ * fa_mha.h -- C ABI of the GB300 (sm_103a) fused multi-head attention forward,
+ * without KV cache (fa_mha_no_cache*) and over a KV cache (fa_mha_kv_cache).
  *
  * The operation is the `mo.mha.no_cache` operator documented on the MAX API
  * page "FlashAttentionGPU" (method `execute`, Steps -1 to 4, and its
@@ -134,6 +134,56 @@ fa_status_t fa_mha_no_cache_noalloc(void *out, float *lse, const void *q, const 
                                     const void *v, int B, int S, int H, int Hkv, int D,
                                     float scale, int mask_kind, int local_window_size,
                                     void *stream, int check_status);
+
+/*
+ * fa_mha_kv_cache -- attention over a KV cache (bf16, tensor cores). The
+ * pages document only the no-cache operator; this is its cached sibling read
+ * the plain way: the same operator (FlashAttentionGPU.execute, Steps -1 to 4)
+ * when the keys and values of batch b are the first L_b = cache_lens[b] rows
+ * of a cache and the Sq queries are the last Sq tokens of that sequence, so
+ * query row s sits at position L_b - Sq + s and the mask (causal: keys j <=
+ * position; window W: position - j < W, or |position - j| < W without the
+ * causal mask) is evaluated there. Sq = 1 is one decoding step; Sq > 1 covers
+ * speculative or chunked steps.
+ *
+ *   out     : device, [B, Sq, H, D] bf16 (BSHD).
+ *   lse     : device, [B, H, Sq] fp32, or NULL (natural log, scale included).
+ *   q       : device, [B, Sq, H, D] bf16 (BSHD).
+ *   k_cache, v_cache : device, [B, S_cache, Hkv, D] bf16 (BShD); rows at
+ *             positions >= L_b are never used (they may hold anything).
+ *   cache_lens : device, B int32 key counts (values outside [0, S_cache] are
+ *             clamped into it), or NULL for S_cache keys in every batch.
+ *   B, Sq, S_cache, H, Hkv, D : sizes; all >= 1, H % Hkv == 0,
+ *             H / Hkv <= 128, D in {64, 128}.
+ *   scale, mask_kind, local_window_size : as fa_mha_no_cache.
+ *   num_splits : 0 picks the number of key-range splits from the device's SM
+ *             count; n >= 1 asks for n (capped at the number of key tiles).
+ *   workspace, workspace_bytes : caller-owned device scratch of at least the
+ *             size fa_mha_kv_cache_plan returns for the same arguments (may be
+ *             NULL when that size is 0); 16-byte aligned.
+ *   dtype   : FA_DTYPE_BF16 (the only type this entry point takes).
+ *   stream  : cudaStream_t as void*.
+ *
+ * A query that sees no key (L_b = 0, or a causal row whose position L_b - Sq
+ * + s is negative) gets out = 0 and lse = -inf. Behaviour on errors and
+ * time-outs is that of fa_mha_no_cache.
+ */
+fa_status_t fa_mha_kv_cache(void *out, float *lse, const void *q, const void *k_cache,
+                            const void *v_cache, const int *cache_lens, int B, int Sq,
+                            int S_cache, int H, int Hkv, int D, float scale, int mask_kind,
+                            int local_window_size, int num_splits, void *workspace,
+                            unsigned long long workspace_bytes, int dtype, void *stream);
+
+/*
+ * fa_mha_kv_cache_plan -- how fa_mha_kv_cache will cut the work for these
+ * arguments: *splits_out receives the number of key-range splits and
+ * *workspace_bytes_out the scratch it needs (0 when there is one split).
+ * num_sms = 0 uses the current device's SM count (the one fa_mha_kv_cache
+ * uses); n >= 1 plans for a device with n SMs and makes no CUDA call.
+ */
+fa_status_t fa_mha_kv_cache_plan(int B, int Sq, int S_cache, int H, int Hkv, int D, int mask_kind,
+                                 int local_window_size, int num_splits, int num_sms,
+                                 int *splits_out, unsigned long long *workspace_bytes_out);
 
 /*
  * fa_device_status -- synchronises `device` (cudaDeviceSynchronize) and reads

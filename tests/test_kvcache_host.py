@@ -1,0 +1,114 @@
+"""Host logic of the KV-cache entry points, without a GPU: the work plan
+(split count, workspace size) and the argument checks that run before any
+CUDA call."""
+import ctypes
+
+import pytest
+
+import attention_fa2_forward_gb300 as fa
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa.build()
+    return fa.load_library()
+
+
+def _plan(*a, **kw):
+    kw.setdefault("num_sms", 152)
+    return fa.kv_cache_plan(*a, **kw)
+
+
+def _tiles(S):
+    return (S + 127) // 128
+
+
+def _expected_splits(req, tiles):
+    """Splits after evening out: every split takes ceil(tiles / req) tiles."""
+    req = min(req, 128, tiles)
+    per = -(-tiles // req)
+    return -(-tiles // per)
+
+
+def test_enough_units_take_one_split():
+    # 16 batches x 8 KV heads = 128 units: one split, no workspace.
+    assert _plan(16, 1, 8192, 32, 8, 128) == (1, 0)
+
+
+@pytest.mark.parametrize("B,Hkv,S", [(1, 8, 131072), (2, 8, 32768), (1, 1, 65536), (4, 4, 8192)])
+def test_few_units_are_split_to_fill_the_gpu(B, Hkv, S):
+    splits, ws = _plan(B, 1, S, 8 * Hkv, Hkv, 128)
+    units = B * Hkv
+    assert splits == _expected_splits(max(1, round(152 / units)), _tiles(S))
+    rows = B * 8 * Hkv
+    expect = ((splits * rows * 128 * 4 + 255) // 256 * 256) + ((splits * rows * 4 + 255) // 256 * 256)
+    assert ws == expect
+
+
+@pytest.mark.parametrize("req", [1, 2, 3, 7, 64, 200])
+def test_requested_splits_are_capped_and_cover_every_tile(req):
+    S = 5000
+    splits, _ = _plan(1, 1, S, 8, 2, 128, num_splits=req)
+    tiles = _tiles(S)
+    assert 1 <= splits <= min(req, 128, tiles)
+    assert splits == _expected_splits(req, tiles)  # no trailing split without tiles
+
+
+def test_window_bounds_the_tiles_to_split():
+    # A causal window of 4096 keys spans at most 33 tiles of 128 keys.
+    splits, _ = _plan(1, 1, 131072, 32, 8, 128, "causal", 4096)
+    assert splits <= 33
+    splits_none, _ = _plan(1, 1, 131072, 32, 8, 128, "none", 4096)
+    assert splits_none <= 65
+
+
+def test_position_tiles_count_as_units():
+    # Sq = 64 with 4 heads per KV head: 2 position tiles of 32 positions.
+    s1, _ = _plan(1, 64, 16384, 8, 2, 128)
+    s2, _ = _plan(1, 32, 16384, 8, 2, 128)
+    assert s1 == _expected_splits(round(152 / 4), 128)
+    assert s2 == _expected_splits(round(152 / 2), 128)
+
+
+P = 0x10000  # a non-null, 16-byte aligned fake address: never dereferenced
+
+
+def _call(lib, out=P, q=P, k=P, v=P, lens=None, B=1, Sq=1, S=256, H=8, Hkv=2, D=128,
+          scale=0.1, mask=1, window=-1, splits=0, ws=None, ws_bytes=0, dtype=0, lse=None):
+    return lib.fa_mha_kv_cache(out, lse, q, k, v, lens, B, Sq, S, H, Hkv, D, scale, mask, window,
+                               splits, ws, ws_bytes, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(k=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Sq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(S=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=6, Hkv=4), fa.FA_ERR_INVALID_ARG),
+    (dict(mask=3), fa.FA_ERR_INVALID_ARG),
+    (dict(window=0), fa.FA_ERR_INVALID_ARG),
+    (dict(splits=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.5), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=1), fa.FA_ERR_UNSUPPORTED),
+    (dict(H=258, Hkv=1), fa.FA_ERR_UNSUPPORTED),  # more than 128 query heads per KV head
+    (dict(q=P + 8), fa.FA_ERR_UNSUPPORTED),
+    (dict(lens=P + 2), fa.FA_ERR_UNSUPPORTED),
+    (dict(S=1 << 30, Hkv=64, H=64), fa.FA_ERR_UNSUPPORTED),
+])
+def test_kv_cache_argument_validation_happens_before_cuda(lib, kw, code):
+    assert _call(lib, **kw) == code
+    assert lib.fa_last_error_message()
+
+
+def test_plan_rejects_bad_arguments(lib):
+    s, w = ctypes.c_int(0), ctypes.c_ulonglong(0)
+    assert lib.fa_mha_kv_cache_plan(1, 1, 256, 8, 2, 128, 1, -1, 0, 152, None,
+                                    ctypes.byref(w)) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_mha_kv_cache_plan(1, 1, 256, 8, 2, 128, 1, -1, 0, -1, ctypes.byref(s),
+                                    ctypes.byref(w)) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_mha_kv_cache_plan(1, 1, 256, 8, 2, 64, 1, -1, 0, 152, ctypes.byref(s),
+                                    ctypes.byref(w)) == fa.FA_OK
+    assert s.value == 1 and w.value == 0 or s.value > 1
