@@ -17,6 +17,7 @@ mask "none", "causal", or causal with a sliding window of W keys.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -194,12 +195,24 @@ def kv_cache_plan(B: int, Sq: int, S_cache: int, H: int, Hkv: int, D: int, mask=
     """(splits, workspace bytes) that :func:`mha_kv_cache` uses for these sizes.
     ``num_sms`` = 0 plans for the current device; n > 0 for an n-SM device
     (no CUDA call)."""
+    if num_sms == 0:
+        num_sms = _sm_count(torch.cuda.current_device())
+    return _kv_cache_plan(int(B), int(Sq), int(S_cache), int(H), int(Hkv), int(D),
+                          _mask_code(mask), int(window), int(num_splits), int(num_sms))
+
+
+@functools.lru_cache(maxsize=None)
+def _sm_count(device: int) -> int:
+    return torch.cuda.get_device_properties(device).multi_processor_count
+
+
+@functools.lru_cache(maxsize=256)
+def _kv_cache_plan(B, Sq, S_cache, H, Hkv, D, mask_code, window, num_splits, num_sms):
     lib = load_library()
     splits = ctypes.c_int(0)
     ws = ctypes.c_ulonglong(0)
-    _check(lib.fa_mha_kv_cache_plan(int(B), int(Sq), int(S_cache), int(H), int(Hkv), int(D),
-                                    _mask_code(mask), int(window), int(num_splits), int(num_sms),
-                                    ctypes.byref(splits), ctypes.byref(ws)))
+    _check(lib.fa_mha_kv_cache_plan(B, Sq, S_cache, H, Hkv, D, mask_code, window, num_splits,
+                                    num_sms, ctypes.byref(splits), ctypes.byref(ws)))
     return int(splits.value), int(ws.value)
 
 

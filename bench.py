@@ -38,6 +38,11 @@ if ROOT not in sys.path:
 DEFAULT_WORKLOAD = "gqa_s4096_d128"
 METRIC = "attention fwd TFLOP/s (unmasked FLOPs) and % of GB300 BF16 tensor peak"
 L2_FLUSH_BYTES = 256 << 20
+# GPU spin (clock cycles, ~100 us) enqueued before each timed step's start
+# event: the GPU stays busy while the host enqueues the step, so the event pair
+# brackets the step's kernels and not host launch latency (which the e2e
+# number includes).
+SPIN_CYCLES = 200_000
 KERNEL_NAME = "fa_fwd_bf16_tc_kernel"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -360,6 +365,7 @@ def bench_ours(args, w, world, rank, local, dist):
     t_wall = time.perf_counter()
     for s in range(args.steps):
         flush.zero_()
+        torch.cuda._sleep(SPIN_CYCLES)
         starts[s].record(stream)
         step()
         ends[s].record(stream)
@@ -439,6 +445,8 @@ def bench_ours(args, w, world, rank, local, dist):
         "config": {"workload": w.name, "shape": w.describe(), "B": w.B, "S": w.S, "H": w.H,
                    "Hkv": w.Hkv, "D": w.D, "mask": mask, "window": w.window,
                    "flops_per_step": flops, "l2": "flushed (256 MiB write) before every step",
+                   "timing": "CUDA events around each step; a GPU spin before the start event "
+                             "hides host launch latency (e2e includes it)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": 100.0 * value / (peak * world),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
@@ -526,6 +534,7 @@ def bench_kv_ours(args, w, world, rank, local, dist):
     clocks.start()
     for s in range(args.steps):
         flush.zero_()
+        torch.cuda._sleep(SPIN_CYCLES)
         starts[s].record(stream)
         step()
         ends[s].record(stream)
@@ -595,6 +604,8 @@ def bench_kv_ours(args, w, world, rank, local, dist):
                    "window": w.window, "lens": "ragged" if w.ragged else "full",
                    "splits": splits, "bytes_per_step": byts, "flops_per_step": flops,
                    "l2": "flushed (256 MiB write) before every step",
+                   "timing": "CUDA events around each step; a GPU spin before the start event "
+                             "hides host launch latency (e2e includes it)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "clocks": clocks.summary(), "gpu_launches": args.steps * (2 if splits > 1 else 1),
