@@ -43,6 +43,17 @@ fa_status_t cuda_fail(cudaError_t err, const char* what) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// bf16 runs any D that is a multiple of 8 (16-byte rows for TMA) up to 128 on
+// the 64- or 128-column tensor-core kernels; fp32 has warp kernels for D/32
+// columns per lane.
+bool head_dim_supported(int D, int dtype) {
+  if (dtype == FA_DTYPE_BF16) return D >= 8 && D <= 256 && D % 8 == 0;
+  return D == 32 || D == 64 || D == 96 || D == 128;
+}
+
+// Columns the tensor-core kernels work on for a head dim D.
+int padded_head_dim(int D) { return D <= 64 ? 64 : (D <= 128 ? 128 : 256); }
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -134,9 +145,13 @@ fa_status_t forward(void* out, float* lse, const void* q, const void* k, const v
     return fail(FA_ERR_INVALID_ARG, "scale must be finite");
   if (scale < 0.f)
     return fail(FA_ERR_UNSUPPORTED, "negative scale is not supported");
-  if (D != 64 && D != 128) return fail(FA_ERR_UNSUPPORTED, "head dim D=%d (built: 64, 128)", D);
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F32)
     return fail(FA_ERR_UNSUPPORTED, "dtype %d", dtype);
+  if (!head_dim_supported(D, dtype))
+    return fail(FA_ERR_UNSUPPORTED, "head dim D=%d (bf16: multiples of 8 up to 256; fp32: 32, 64, "
+                "96, 128)", D);
+  if (dtype == FA_DTYPE_BF16 && D > 128 && H / Hkv > 128)
+    return fail(FA_ERR_UNSUPPORTED, "D > 128 needs H / Hkv <= 128 (got %d)", H / Hkv);
   const long long elems_q = static_cast<long long>(B) * S * H * D;
   const long long row_bytes = static_cast<long long>(S) * H * D * 2;
   if (elems_q >= (1ll << 40) || row_bytes >= (1ll << 39) ||
@@ -199,7 +214,41 @@ fa_status_t forward(void* out, float* lse, const void* q, const void* k, const v
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dtype == FA_DTYPE_BF16) {
+  if (dtype == FA_DTYPE_BF16 && D > 128) {
+    // Head dims above 128 run on the one-Q-tile kernel of the KV-cache path
+    // (S double-buffered in tensor-memory columns 0-255, O in 256-511) with
+    // every key present: Sq = S_cache = S, one split.
+    fa::DecodeProblem dp{};
+    dp.B = B;
+    dp.Sq = S;
+    dp.Scache = S;
+    dp.H = H;
+    dp.Hkv = Hkv;
+    dp.D = D;
+    dp.G = H / Hkv;
+    dp.Pq = S < 128 / dp.G ? S : 128 / dp.G;
+    dp.R = dp.G * dp.Pq;
+    dp.n_ptiles = (S + dp.Pq - 1) / dp.Pq;
+    dp.causal = p.causal;
+    dp.window = p.window;
+    dp.scale = p.scale;
+    dp.scale_log2 = p.scale_log2;
+    dp.lens = nullptr;
+    dp.splits = 1;
+    dp.tiles_per_split = (S + 127) / 128;
+    dp.lse = lse;
+    dp.status = status;
+    dp.wait_limit_ns = p.wait_limit_ns;
+    dp.stall_probe = p.stall_probe;
+    dp.sq = p.sq;
+    dp.sk = p.sk;
+    dp.sv = p.sv;
+    dp.so = p.so;
+    if (static_cast<long long>(Hkv) * dp.n_ptiles * B > 0x7fffffffll)
+      return fail(FA_ERR_UNSUPPORTED, "problem too large (grid)");
+    err = fa::launch_decode_bf16_tc(dp, out, q, k, v, s);
+    if (err != cudaSuccess) return cuda_fail(err, "bf16 tensor-core kernel launch (D > 128)");
+  } else if (dtype == FA_DTYPE_BF16) {
     err = fa::launch_fwd_bf16_tc(p, out, q, k, v, s);
     if (err != cudaSuccess) return cuda_fail(err, "bf16 tensor-core kernel launch");
   } else {
@@ -238,7 +287,8 @@ fa_status_t check_kv_args(int B, int Sq, int S_cache, int H, int Hkv, int D, int
     return fail(FA_ERR_INVALID_ARG, "local_window_size must be -1 or >= 1 (got %d)",
                 local_window_size);
   if (num_splits < 0) return fail(FA_ERR_INVALID_ARG, "num_splits must be >= 0");
-  if (D != 64 && D != 128) return fail(FA_ERR_UNSUPPORTED, "head dim D=%d (built: 64, 128)", D);
+  if (!head_dim_supported(D, FA_DTYPE_BF16))
+    return fail(FA_ERR_UNSUPPORTED, "head dim D=%d (multiples of 8 up to 256)", D);
   if (H / Hkv > 128)
     return fail(FA_ERR_UNSUPPORTED, "H / Hkv = %d query heads per KV head (at most 128)", H / Hkv);
   const long long q_elems = static_cast<long long>(B) * Sq * H * D;
@@ -268,10 +318,13 @@ KvPlan make_kv_plan(int B, int Sq, int S_cache, int H, int Hkv, int D, int causa
   }
   long long splits = num_splits;
   if (splits == 0) {
-    // Auto: enough CTAs (one per SM at most) to fill the GPU once.
+    // Auto. Units (batch x KV head x position tile) that fill half the SMs
+    // stream best unsplit (one CTA each, no combine). Fewer units are cut so
+    // that about 1.5 CTAs per SM exist: enough for the HBM stream, and when
+    // the lengths are ragged (unknown here: they live on the device) the
+    // splits of short sequences finish early and free their SMs for others.
     const long long units = static_cast<long long>(B) * Hkv * k.n_ptiles;
-    splits = (num_sms + units / 2) / units;
-    if (splits < 1) splits = 1;
+    splits = 2 * units >= num_sms ? 1 : (3ll * num_sms + 2 * units - 1) / (2 * units);
   }
   if (splits > kMaxSplits) splits = kMaxSplits;
   if (splits > max_tiles) splits = max_tiles;
@@ -279,7 +332,8 @@ KvPlan make_kv_plan(int B, int Sq, int S_cache, int H, int Hkv, int D, int causa
   k.splits = static_cast<int>((max_tiles + k.tiles_per_split - 1) / k.tiles_per_split);
   if (k.splits > 1) {
     const unsigned long long rows = static_cast<unsigned long long>(B) * Sq * H;
-    k.o_part_bytes = align256(k.splits * rows * D * 4ull);
+    const unsigned long long d_pad = padded_head_dim(D);  // the kernel's padded row
+    k.o_part_bytes = align256(k.splits * rows * d_pad * 4ull);
     k.workspace_bytes = k.o_part_bytes + align256(k.splits * rows * 4ull);
   }
   return k;

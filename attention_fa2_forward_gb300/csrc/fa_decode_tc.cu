@@ -58,10 +58,13 @@ constexpr unsigned long long kDrainExtraNs = 100000000ull;  // 100 ms
 
 template <int D>
 struct DCfg {
-  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(D == 64 || D == 128 || D == 256, "head dim");
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kBoxes * kBoxBytes;
-  static constexpr int kStages = D == 128 ? 6 : 10;
+  // Ring slots: what fits next to the Q tile in 227 KB. Two slots suffice for
+  // the ring order (K0 K1 | V0 K2 | ...): each refill waits only on an MMA
+  // that needs nothing later in the ring.
+  static constexpr int kStages = D == 256 ? 2 : (D == 128 ? 6 : 10);
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
@@ -107,7 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   id /= static_cast<unsigned>(p.splits);
   const int hk = static_cast<int>(id % static_cast<unsigned>(p.Hkv));
   id /= static_cast<unsigned>(p.Hkv);
-  const int pt = static_cast<int>(id % static_cast<unsigned>(p.n_ptiles));
+  // Later position tiles see more keys under the causal mask: start them first.
+  const int pt = p.n_ptiles - 1 - static_cast<int>(id % static_cast<unsigned>(p.n_ptiles));
   const int b = static_cast<int>(id / static_cast<unsigned>(p.n_ptiles));
 
   const int L = min(max(p.lens != nullptr ? p.lens[b] : p.Scache, 0), p.Scache);
@@ -523,6 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merges the splits' partial results: one warp per output row (b, s, h).
+// Partial rows hold D (padded) floats; out rows hold the real p.D <= D.
 // O = sum_i w_i O_i / sum_i w_i and LSE = M + ln(sum_i w_i), with
 // w_i = exp(LSE_i - M), M = max_i LSE_i; splits that saw no key (LSE_i = -inf)
 // are skipped, and a row no split saw gets O = 0, LSE = -inf.
@@ -559,12 +564,15 @@ __global__ void __launch_bounds__(256)
       const float* src =
           p.o_part + ((((static_cast<size_t>(s) * p.B + b) * p.Sq + sq) * p.H + h) * D) +
           lane * kPer;
-      if constexpr (kPer == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        acc[0] = fmaf(w, x.x, acc[0]);
-        acc[1] = fmaf(w, x.y, acc[1]);
-        acc[2] = fmaf(w, x.z, acc[2]);
-        acc[3] = fmaf(w, x.w, acc[3]);
+      if constexpr (kPer % 4 == 0) {
+#pragma unroll
+        for (int u = 0; u < kPer; u += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src + u);
+          acc[u] = fmaf(w, x.x, acc[u]);
+          acc[u + 1] = fmaf(w, x.y, acc[u + 1]);
+          acc[u + 2] = fmaf(w, x.z, acc[u + 2]);
+          acc[u + 3] = fmaf(w, x.w, acc[u + 3]);
+        }
       } else {
         const float2 x = *reinterpret_cast<const float2*>(src);
         acc[0] = fmaf(w, x.x, acc[0]);
@@ -573,14 +581,20 @@ __global__ void __launch_bounds__(256)
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  __nv_bfloat16* dst = out + ((static_cast<size_t>(b) * p.Sq + sq) * p.H + h) * D + lane * kPer;
-  if constexpr (kPer == 4) {
-    uint2 pk;
-    pk.x = ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    pk.y = ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    *reinterpret_cast<uint2*>(dst) = pk;
-  } else {
-    *reinterpret_cast<uint32_t*>(dst) = ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  __nv_bfloat16* dst = out + static_cast<size_t>(b) * p.so.b + static_cast<size_t>(sq) * p.so.s +
+                       static_cast<size_t>(h) * p.so.h + lane * kPer;
+  if (lane * kPer + kPer <= p.D) {  // p.D is a multiple of 8: whole groups
+    if constexpr (kPer % 4 == 0) {
+#pragma unroll
+      for (int u = 0; u < kPer; u += 4) {
+        uint2 pk;
+        pk.x = ptx::pack_bf16x2(acc[u] * inv, acc[u + 1] * inv);
+        pk.y = ptx::pack_bf16x2(acc[u + 2] * inv, acc[u + 3] * inv);
+        *reinterpret_cast<uint2*>(dst + u) = pk;
+      }
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
   }
   if (lane == 0 && p.lse != nullptr)
     p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + sq] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
@@ -590,10 +604,12 @@ template <int D>
 cudaError_t launch_d(const DecodeProblem& p, void* out, const void* q, const void* k,
                      const void* v, cudaStream_t stream) {
   CUtensorMap tq, tk, tv, to;
-  if (!encode_bshd_tensor_map(&tq, q, p.B, p.Sq, p.H, D, BshdStrides{}, p.G, p.Pq) ||
-      !encode_bshd_tensor_map(&tk, k, p.B, p.Scache, p.Hkv, D, BshdStrides{}) ||
-      !encode_bshd_tensor_map(&tv, v, p.B, p.Scache, p.Hkv, D, BshdStrides{}) ||
-      !encode_bshd_tensor_map(&to, out, p.B, p.Sq, p.H, D, BshdStrides{}, p.G, p.Pq))
+  // The maps carry the real head dim p.D <= D (padding columns: zero-filled
+  // on load, clipped on store).
+  if (!encode_bshd_tensor_map(&tq, q, p.B, p.Sq, p.H, p.D, p.sq, p.G, p.Pq) ||
+      !encode_bshd_tensor_map(&tk, k, p.B, p.Scache, p.Hkv, p.D, p.sk) ||
+      !encode_bshd_tensor_map(&tv, v, p.B, p.Scache, p.Hkv, p.D, p.sv) ||
+      !encode_bshd_tensor_map(&to, out, p.B, p.Sq, p.H, p.D, p.so, p.G, p.Pq))
     return cudaErrorInvalidValue;
   const long long grid = static_cast<long long>(p.splits) * p.Hkv * p.n_ptiles * p.B;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
@@ -608,8 +624,10 @@ cudaError_t launch_d(const DecodeProblem& p, void* out, const void* q, const voi
   const long long rows = static_cast<long long>(p.B) * p.Sq * p.H;
   const long long cgrid = (rows + 7) / 8;
   if (cgrid > INT_MAX) return cudaErrorInvalidConfiguration;
+  DecodeProblem pc = p;  // the combine kernel addresses out with resolved strides
+  pc.so = resolve_strides(p.so, p.Sq, p.H, p.D);
   fa_decode_combine_kernel<D><<<static_cast<unsigned>(cgrid), 256, 0, stream>>>(
-      p, static_cast<__nv_bfloat16*>(out));
+      pc, static_cast<__nv_bfloat16*>(out));
   return cudaGetLastError();
 }
 
@@ -617,8 +635,10 @@ cudaError_t launch_d(const DecodeProblem& p, void* out, const void* q, const voi
 
 cudaError_t launch_decode_bf16_tc(const DecodeProblem& p, void* out, const void* q, const void* k,
                                   const void* v, cudaStream_t stream) {
-  if (p.D == 64) return launch_d<64>(p, out, q, k, v, stream);
-  if (p.D == 128) return launch_d<128>(p, out, q, k, v, stream);
+  if (p.D % 8 != 0 || p.D < 8 || p.D > 256) return cudaErrorInvalidValue;
+  if (p.D <= 64) return launch_d<64>(p, out, q, k, v, stream);
+  if (p.D <= 128) return launch_d<128>(p, out, q, k, v, stream);
+  return launch_d<256>(p, out, q, k, v, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -133,8 +133,13 @@ cudaError_t launch_d(const FwdProblem& p, float* out, const float* q, const floa
 
 cudaError_t launch_fwd_f32_simt(const FwdProblem& p, float* out, const float* q, const float* k,
                                 const float* v, cudaStream_t stream) {
-  if (p.D == 64) return launch_d<64>(p, out, q, k, v, stream);
-  if (p.D == 128) return launch_d<128>(p, out, q, k, v, stream);
+  switch (p.D) {
+    case 32: return launch_d<32>(p, out, q, k, v, stream);
+    case 64: return launch_d<64>(p, out, q, k, v, stream);
+    case 96: return launch_d<96>(p, out, q, k, v, stream);
+    case 128: return launch_d<128>(p, out, q, k, v, stream);
+    default: return cudaErrorInvalidValue;
+  }
   return cudaErrorInvalidValue;
 }
 

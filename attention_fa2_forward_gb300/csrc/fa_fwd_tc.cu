@@ -478,10 +478,13 @@ template <int D>
 cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* k, const void* v,
                      cudaStream_t stream) {
   CUtensorMap tq, tk, tv, to;
-  if (!encode_bshd_tensor_map(&tq, q, p.B, p.S, p.H, D, p.sq) ||
-      !encode_bshd_tensor_map(&tk, k, p.B, p.S, p.Hkv, D, p.sk) ||
-      !encode_bshd_tensor_map(&tv, v, p.B, p.S, p.Hkv, D, p.sv) ||
-      !encode_bshd_tensor_map(&to, out, p.B, p.S, p.H, D, p.so))
+  // The maps carry the real head dim p.D <= D: loads zero-fill columns
+  // p.D..D-1 (adding nothing to Q K^T and giving zero O columns) and the
+  // store clips them.
+  if (!encode_bshd_tensor_map(&tq, q, p.B, p.S, p.H, p.D, p.sq) ||
+      !encode_bshd_tensor_map(&tk, k, p.B, p.S, p.Hkv, p.D, p.sk) ||
+      !encode_bshd_tensor_map(&tv, v, p.B, p.S, p.Hkv, p.D, p.sv) ||
+      !encode_bshd_tensor_map(&to, out, p.B, p.S, p.H, p.D, p.so))
     return cudaErrorInvalidValue;
   const int nqb = (p.S + kQTiles * kBM - 1) / (kQTiles * kBM);
   const long long grid = static_cast<long long>(nqb) * p.H * p.B;
@@ -499,8 +502,10 @@ cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* 
 
 cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, const void* k,
                                const void* v, cudaStream_t stream) {
-  if (p.D == 64) return launch_d<64>(p, out, q, k, v, stream);
-  if (p.D == 128) return launch_d<128>(p, out, q, k, v, stream);
+  // Head dims up to 64 (128) run on the 64 (128) column kernel.
+  if (p.D % 8 != 0 || p.D < 8 || p.D > 128) return cudaErrorInvalidValue;
+  if (p.D <= 64) return launch_d<64>(p, out, q, k, v, stream);
+  return launch_d<128>(p, out, q, k, v, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -60,6 +60,7 @@ struct DecodeProblem {
   unsigned* status;
   unsigned long long wait_limit_ns;
   int stall_probe;
+  BshdStrides sq, sk, sv, so;  // layouts of q, the caches and out (zero: dense)
 };
 
 // Launches the KV-cache kernel (and, with splits > 1, the combine kernel).

@@ -87,7 +87,8 @@ extern "C" fa_status_t fa_mha_no_cache_noalloc(void* out, float* lse, const void
     return noalloc_fail(FA_ERR_INVALID_ARG, "bad local_window_size %d", local_window_size);
   if (!std::isfinite(scale)) return noalloc_fail(FA_ERR_INVALID_ARG, "scale must be finite");
   if (scale < 0.f) return noalloc_fail(FA_ERR_UNSUPPORTED, "negative scale");
-  if (D != 64 && D != 128) return noalloc_fail(FA_ERR_UNSUPPORTED, "head dim D=%d", D);
+  if (D < 8 || D > 128 || D % 8 != 0)
+    return noalloc_fail(FA_ERR_UNSUPPORTED, "head dim D=%d (multiples of 8 up to 128)", D);
   const long long elems_q = static_cast<long long>(B) * S * H * D;
   if (elems_q >= (1ll << 40) || static_cast<long long>(S) * H * D * 2 >= (1ll << 39) ||
       static_cast<long long>(B) * H * ((S + 255) / 256) > 0x7fffffffll)

@@ -45,7 +45,7 @@ class Workload:
                 f"{self.dtype} {mask}")
 
 
-# The five workloads: a tiny fp32 case the oracle finishes instantly, a short
+# The workloads: a tiny fp32 case the oracle finishes instantly, a short
 # causal MHA case, a causal GQA case, a sliding-window GQA case and a
 # long-context multi-query stress case with large logits.
 WORKLOADS = {
@@ -56,6 +56,9 @@ WORKLOADS = {
                                  window=4096, seed=1003),
     "mqa_s32768_stress": Workload("mqa_s32768_stress", 1, 32768, 16, 1, 128, "bf16", True,
                                   q_std=3.0, k_std=3.0, v_dist="uniform", seed=1004),
+    # Other head dims: 96 (padded to the 128-column kernel), 256 (one-Q-tile kernel).
+    "gqa_s4096_d96": Workload("gqa_s4096_d96", 2, 4096, 32, 8, 96, "bf16", True, seed=1005),
+    "gqa_s4096_d256": Workload("gqa_s4096_d256", 2, 4096, 16, 8, 256, "bf16", True, seed=1006),
 }
 
 

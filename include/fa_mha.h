@@ -56,7 +56,11 @@ typedef enum {
  *           statistic a split-KV combine consumes).
  *   q     : device, [B, S, H, D] (BSHD).
  *   k, v  : device, [B, S, Hkv, D] (BSHD when Hkv == H, BShD otherwise).
- *   B, S, H, Hkv, D : sizes; B, S, H, Hkv >= 1, H % Hkv == 0, D in {64, 128}.
+ *   B, S, H, Hkv, D : sizes; B, S, H, Hkv >= 1, H % Hkv == 0. D: for
+ *           FA_DTYPE_BF16 a multiple of 8 up to 256 (the kernels work on 64,
+ *           128 or 256 columns; TMA zero-fills the rest and clips it on store;
+ *           above 128 also H / Hkv <= 128), for FA_DTYPE_F32 one of 32, 64, 96,
+ *           128.
  *   scale : multiplies q.k before masking and softmax (the page's `scale`);
  *           finite and >= 0.
  *   mask_kind : FA_MASK_NONE or FA_MASK_CAUSAL.
@@ -154,7 +158,7 @@ fa_status_t fa_mha_no_cache_noalloc(void *out, float *lse, const void *q, const 
  *   cache_lens : device, B int32 key counts (values outside [0, S_cache] are
  *             clamped into it), or NULL for S_cache keys in every batch.
  *   B, Sq, S_cache, H, Hkv, D : sizes; all >= 1, H % Hkv == 0,
- *             H / Hkv <= 128, D in {64, 128}.
+ *             H / Hkv <= 128, D a multiple of 8 up to 256.
  *   scale, mask_kind, local_window_size : as fa_mha_no_cache.
  *   num_splits : 0 picks the number of key-range splits from the device's SM
  *             count; n >= 1 asks for n (capped at the number of key tiles).

@@ -69,7 +69,10 @@ def _call(lib, out=P, lse=None, q=P, k=P, v=P, B=1, S=8, H=2, Hkv=2, D=64, scale
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=-1.0), fa.FA_ERR_UNSUPPORTED),
-    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=100), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=264), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=256, H=258, Hkv=1), fa.FA_ERR_UNSUPPORTED),  # D > 128 needs H / Hkv <= 128
+    (dict(D=80, dtype=1), fa.FA_ERR_UNSUPPORTED),  # fp32: D in {32, 64, 96, 128}
     (dict(dtype=7), fa.FA_ERR_UNSUPPORTED),
     (dict(q=P + 8), fa.FA_ERR_UNSUPPORTED),  # bf16 tensors need 16-byte alignment
     (dict(S=1 << 30, H=1 << 10), fa.FA_ERR_UNSUPPORTED),

@@ -94,6 +94,13 @@ def test_kv_cache_matches_oracle(oracle_mod, case, num_splits):
     _case(oracle_mod, *case, num_splits=num_splits, seed=11 + CASES.index(case))
 
 
+@pytest.mark.parametrize("D", [16, 32, 80, 96, 112, 136, 256])
+@pytest.mark.parametrize("num_splits", [1, 3])
+def test_kv_cache_other_head_dims(oracle_mod, D, num_splits):
+    _case(oracle_mod, 2, 3, 700, 8, 2, D, [700, 333], True, -1, num_splits=num_splits,
+          seed=50 + D)
+
+
 @pytest.mark.parametrize("num_splits", [2, 5, 8, 64])
 def test_many_splits_on_a_long_cache(oracle_mod, num_splits):
     _case(oracle_mod, 2, 1, 5000, 8, 2, 128, [5000, 3333], True, -1, num_splits=num_splits)

@@ -100,7 +100,8 @@ def _sample_rows(S, seed, n_random=40):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["gqa_s4096_d128", "swa_s16384_w4096", "mqa_s32768_stress"])
+@pytest.mark.parametrize("name", ["gqa_s4096_d128", "swa_s16384_w4096", "mqa_s32768_stress",
+                                  "gqa_s4096_d96", "gqa_s4096_d256"])
 def test_full_size_workload_sampled_rows(oracle_mod, name):
     w = WORKLOADS[name]
     q, k, v = workload_inputs(w)
@@ -146,6 +147,37 @@ EDGE_SHAPES = [
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 def test_edge_shapes(oracle_mod, S, H, Hkv, D, causal, window, dtype):
     _full_case(oracle_mod, 2, S, H, Hkv, D, dtype, causal, window, seed=7 + S)
+
+
+# Head dims other than 64 and 128: bf16 runs any multiple of 8 up to 128 on the
+# 64- or 128-column kernel (zero-filled padding columns) and up to 256 on the
+# one-Q-tile kernel; fp32 has 32 and 96.
+HEAD_DIMS_BF16 = [8, 16, 32, 40, 80, 96, 112, 136, 192, 256]
+
+
+@pytest.mark.parametrize("D", HEAD_DIMS_BF16)
+@pytest.mark.parametrize("causal,window", [(True, -1), (False, -1), (True, 100), (False, 60)])
+def test_other_head_dims_bf16(oracle_mod, D, causal, window):
+    _full_case(oracle_mod, 2, 333, 4, 2, D, torch.bfloat16, causal, window, seed=40 + D)
+
+
+@pytest.mark.parametrize("D", [32, 96])
+@pytest.mark.parametrize("causal,window", [(True, -1), (False, 60)])
+def test_other_head_dims_f32(oracle_mod, D, causal, window):
+    _full_case(oracle_mod, 2, 200, 4, 2, D, torch.float32, causal, window, seed=60 + D)
+
+
+@pytest.mark.parametrize("D,H,Hkv,window", [(96, 16, 4, -1), (256, 8, 2, -1), (256, 4, 4, 700)])
+def test_other_head_dims_long_sampled_rows(oracle_mod, D, H, Hkv, window):
+    B, S = 1, 4100
+    q, k, v = make_qkv(B, S, H, Hkv, D, torch.bfloat16, seed=35 + D)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = _run_gpu(q, k, v, scale, True, window)
+    rows = _sample_rows(S, 35)
+    ref_out, ref_lse = oracle_mod.mha_forward(q[:, rows], k, v, scale, True, window, rows=rows)
+    _compare(out[:, rows], lse[:, :, rows], ref_out, ref_lse, torch.bfloat16,
+             f"S4100 D{D} W{window}")
+    assert np.isfinite(out).all()
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
@@ -208,10 +240,13 @@ def test_ragged_noncausal_whole(oracle_mod):
 # --- strided views (fa_mha_no_cache_strided) ------------------------------------------
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
-def test_packed_qkv_slices_and_strided_output(oracle_mod, dtype):
+@pytest.mark.parametrize("D", [128, 256])
+def test_packed_qkv_slices_and_strided_output(oracle_mod, dtype, D):
     """q, k, v as slices of one packed [B, S, H + 2 Hkv, D] projection; out written
     into a slice of a wider buffer whose other heads must stay untouched."""
-    B, S, H, Hkv, D = 2, 700, 8, 2, 128
+    if dtype == torch.float32 and D > 128:
+        pytest.skip("fp32 head dims stop at 128")
+    B, S, H, Hkv = 2, 700, 8, 2
     q, k, v = make_qkv(B, S, H, Hkv, D, dtype, seed=41)
     dev = torch.device("cuda:0")
     qkv = torch.cat([q, k, v], dim=2).to(dev)

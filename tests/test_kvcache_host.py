@@ -31,15 +31,19 @@ def _expected_splits(req, tiles):
 
 
 def test_enough_units_take_one_split():
-    # 16 batches x 8 KV heads = 128 units: one split, no workspace.
+    # 16 batches x 8 KV heads = 128 units: one split, no workspace; 76 units
+    # (half of 152 SMs) still one.
     assert _plan(16, 1, 8192, 32, 8, 128) == (1, 0)
+    assert _plan(19, 1, 8192, 16, 4, 128) == (1, 0)
+    assert _plan(37, 1, 8192, 8, 2, 128)[0] > 1
 
 
-@pytest.mark.parametrize("B,Hkv,S", [(1, 8, 131072), (2, 8, 32768), (1, 1, 65536), (4, 4, 8192)])
+@pytest.mark.parametrize("B,Hkv,S", [(1, 8, 131072), (2, 8, 32768), (1, 1, 65536), (4, 4, 8192),
+                                     (8, 8, 32768)])
 def test_few_units_are_split_to_fill_the_gpu(B, Hkv, S):
     splits, ws = _plan(B, 1, S, 8 * Hkv, Hkv, 128)
     units = B * Hkv
-    assert splits == _expected_splits(max(1, round(152 / units)), _tiles(S))
+    assert splits == _expected_splits(-(-3 * 152 // (2 * units)), _tiles(S))
     rows = B * 8 * Hkv
     expect = ((splits * rows * 128 * 4 + 255) // 256 * 256) + ((splits * rows * 4 + 255) // 256 * 256)
     assert ws == expect
@@ -66,8 +70,8 @@ def test_position_tiles_count_as_units():
     # Sq = 64 with 4 heads per KV head: 2 position tiles of 32 positions.
     s1, _ = _plan(1, 64, 16384, 8, 2, 128)
     s2, _ = _plan(1, 32, 16384, 8, 2, 128)
-    assert s1 == _expected_splits(round(152 / 4), 128)
-    assert s2 == _expected_splits(round(152 / 2), 128)
+    assert s1 == _expected_splits(-(-3 * 152 // 8), 128)
+    assert s2 == _expected_splits(-(-3 * 152 // 4), 128)
 
 
 P = 0x10000  # a non-null, 16-byte aligned fake address: never dereferenced
@@ -91,7 +95,7 @@ def _call(lib, out=P, q=P, k=P, v=P, lens=None, B=1, Sq=1, S=256, H=8, Hkv=2, D=
     (dict(splits=-1), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=-0.5), fa.FA_ERR_UNSUPPORTED),
-    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=100), fa.FA_ERR_UNSUPPORTED),
     (dict(dtype=1), fa.FA_ERR_UNSUPPORTED),
     (dict(H=258, Hkv=1), fa.FA_ERR_UNSUPPORTED),  # more than 128 query heads per KV head
     (dict(q=P + 8), fa.FA_ERR_UNSUPPORTED),

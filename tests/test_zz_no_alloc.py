@@ -65,5 +65,5 @@ def test_noalloc_rejects_arguments_before_launch():
     fn = _noalloc_fn()
     P = 0x10000
     assert fn(P, None, P, P, P, 1, 8, 3, 2, 64, 0.1, 1, -1, None, 0) == fa.FA_ERR_INVALID_ARG
-    assert fn(P, None, P, P, P, 1, 8, 2, 2, 96, 0.1, 1, -1, None, 0) == fa.FA_ERR_UNSUPPORTED
+    assert fn(P, None, P, P, P, 1, 8, 2, 2, 100, 0.1, 1, -1, None, 0) == fa.FA_ERR_UNSUPPORTED
     assert fa.load_library().fa_last_error_message()
