@@ -38,7 +38,8 @@ FA_ERR_TIMEOUT = 4
 
 # Every symbol the header declares (checked by the tests).
 EXPORTS = ("fa_mha_no_cache", "fa_mha_no_cache_strided", "fa_mha_no_cache_noalloc",
-           "fa_mha_kv_cache", "fa_mha_kv_cache_plan", "fa_device_status",
+           "fa_mha_kv_cache", "fa_mha_kv_cache_plan", "fa_topk", "fa_topk_plan",
+           "fa_device_status",
            "fa_set_wait_timeout_ns", "fa_set_stall_probe", "fa_status_string",
            "fa_last_error_message", "fa_version", "fa_shutdown")
 
@@ -79,6 +80,10 @@ def load_library(path: str | None = None):
         lib.fa_mha_kv_cache_plan.restype = i
         lib.fa_mha_kv_cache_plan.argtypes = [i, i, i, i, i, i, i, i, i, i,
                                              ctypes.POINTER(i), ctypes.POINTER(ull)]
+        lib.fa_topk.restype = i
+        lib.fa_topk.argtypes = [vp, vp, vp, i, i, ctypes.c_longlong, i, vp, ull, vp]
+        lib.fa_topk_plan.restype = i
+        lib.fa_topk_plan.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(ull)]
         lib.fa_device_status.restype = i
         lib.fa_device_status.argtypes = [i, i]
         lib.fa_set_wait_timeout_ns.restype = ctypes.c_ulonglong
@@ -281,6 +286,54 @@ def mha_kv_cache(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
             int(ws_bytes), DTYPE_BF16, st.cuda_stream)
     _check(rc)
     return (out, lse) if return_lse else out
+
+
+def topk_plan(B: int, V: int, K: int, num_sms: int = 0) -> tuple[int, int]:
+    """(chunks per row, workspace bytes) that :func:`topk` uses; ``num_sms`` = 0
+    plans for the current device, n > 0 for an n-SM device (no CUDA call)."""
+    if num_sms == 0:
+        num_sms = _sm_count(torch.cuda.current_device())
+    return _topk_plan(int(B), int(V), int(K), int(num_sms))
+
+
+@functools.lru_cache(maxsize=256)
+def _topk_plan(B, V, K, num_sms):
+    lib = load_library()
+    chunks = ctypes.c_int(0)
+    ws = ctypes.c_ulonglong(0)
+    _check(lib.fa_topk_plan(B, V, K, num_sms, ctypes.byref(chunks), ctypes.byref(ws)))
+    return int(chunks.value), int(ws.value)
+
+
+def topk(scores: torch.Tensor, k: int, *, values: torch.Tensor | None = None,
+         indices: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+         stream: torch.cuda.Stream | None = None):
+    """Exact top-k of each row of a [B, V] fp32 CUDA tensor (last dim
+    contiguous): (values [B, k] fp32 descending in IEEE total order, indices
+    [B, k] int32), equal values by ascending index."""
+    if scores.dim() != 2 or not scores.is_cuda or scores.dtype != torch.float32:
+        raise ValueError("scores must be a 2-D fp32 CUDA tensor")
+    if scores.stride(1) != 1:
+        raise ValueError("scores must have a contiguous last dimension")
+    B, V = scores.shape
+    if values is None:
+        values = torch.empty((B, k), dtype=torch.float32, device=scores.device)
+    if indices is None:
+        indices = torch.empty((B, k), dtype=torch.int32, device=scores.device)
+    for name, t, dt in (("values", values, torch.float32), ("indices", indices, torch.int32)):
+        if t.shape != (B, k) or t.dtype != dt or not t.is_contiguous() or t.device != scores.device:
+            raise ValueError(f"{name} must be a contiguous {dt} [B, k] tensor on scores' device")
+    lib = load_library()
+    with torch.cuda.device(scores.device):
+        _, ws_bytes = topk_plan(B, V, k)
+        if workspace is None or workspace.numel() * workspace.element_size() < ws_bytes:
+            workspace = torch.empty(max(ws_bytes, 8), dtype=torch.uint8, device=scores.device)
+        st = stream if stream is not None else torch.cuda.current_stream(scores.device)
+        rc = lib.fa_topk(values.data_ptr(), indices.data_ptr(), scores.data_ptr(), B, V,
+                         scores.stride(0), int(k), workspace.data_ptr(), int(ws_bytes),
+                         st.cuda_stream)
+    _check(rc)
+    return values, indices
 
 
 def device_status(device: int | None = None, clear: bool = True) -> int:

@@ -348,9 +348,98 @@ fa_status_t current_sm_count(int* out) {
   return FA_OK;
 }
 
+// ---------------------------------------------------------------- top-K
+
+struct TopkPlan {
+  int chunk, n_chunks;
+  unsigned long long workspace_bytes;
+};
+
+// Chunks per row: about two CTAs per SM over the whole batch, chunks of a
+// multiple of 2048 elements (8 warps x 256-element steps), and at most 4096
+// candidates per row for the merge.
+TopkPlan make_topk_plan(int B, int V, int K, int num_sms) {
+  constexpr long long kStep = 2048;
+  long long chunks = (2ll * num_sms + B - 1) / B;
+  const long long by_merge = 4096 / K > 0 ? 4096 / K : 1;
+  if (chunks > by_merge) chunks = by_merge;
+  if (chunks < 1) chunks = 1;
+  long long chunk = (V + chunks - 1) / chunks;
+  chunk = (chunk + kStep - 1) / kStep * kStep;
+  TopkPlan t;
+  t.chunk = static_cast<int>(chunk);
+  t.n_chunks = static_cast<int>((V + chunk - 1) / chunk);
+  t.workspace_bytes = static_cast<unsigned long long>(B) * t.n_chunks * K * 8ull;
+  return t;
+}
+
+fa_status_t check_topk_args(int B, int V, int K) {
+  if (B < 1 || V < 1) return fail(FA_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d V=%d)", B, V);
+  if (K < 1 || K > V) return fail(FA_ERR_INVALID_ARG, "K must be in [1, V] (K=%d V=%d)", K, V);
+  if (K > fa::kMaxTopK) return fail(FA_ERR_UNSUPPORTED, "K=%d (at most %d)", K, fa::kMaxTopK);
+  if (B > 65535) return fail(FA_ERR_UNSUPPORTED, "B=%d rows (at most 65535)", B);
+  if (V > (1 << 30)) return fail(FA_ERR_UNSUPPORTED, "V=%d (at most 2^30)", V);
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+fa_status_t fa_topk_plan(int B, int V, int K, int num_sms, int* chunks_out,
+                         unsigned long long* workspace_bytes_out) {
+  if (chunks_out == nullptr || workspace_bytes_out == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "null output pointer");
+  fa_status_t st = check_topk_args(B, V, K);
+  if (st != FA_OK) return st;
+  if (num_sms < 0) return fail(FA_ERR_INVALID_ARG, "num_sms must be >= 0");
+  if (num_sms == 0 && (st = current_sm_count(&num_sms)) != FA_OK) return st;
+  const TopkPlan t = make_topk_plan(B, V, K, num_sms);
+  *chunks_out = t.n_chunks;
+  *workspace_bytes_out = t.workspace_bytes;
+  return FA_OK;
+}
+
+fa_status_t fa_topk(float* values, int* indices, const float* scores, int B, int V,
+                    long long row_stride, int K, void* workspace,
+                    unsigned long long workspace_bytes, void* stream) {
+  if (values == nullptr || indices == nullptr || scores == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  fa_status_t st = check_topk_args(B, V, K);
+  if (st != FA_OK) return st;
+  if (row_stride < V) return fail(FA_ERR_INVALID_ARG, "row_stride %lld < V %d", row_stride, V);
+  if (row_stride >= (1ll << 40)) return fail(FA_ERR_UNSUPPORTED, "row_stride too large");
+  if (!aligned(values, 4) || !aligned(indices, 4) || !aligned(scores, 4) ||
+      (workspace != nullptr && !aligned(workspace, 8)))
+    return fail(FA_ERR_UNSUPPORTED, "buffers must be 4-byte aligned (workspace 8)");
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  int major = 0, minor = 0, sms = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(FA_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+  if ((st = current_sm_count(&sms)) != FA_OK) return st;
+  const TopkPlan t = make_topk_plan(B, V, K, sms);
+  if (workspace == nullptr || workspace_bytes < t.workspace_bytes)
+    return fail(FA_ERR_INVALID_ARG, "workspace of %llu bytes needed, %llu given",
+                t.workspace_bytes, workspace != nullptr ? workspace_bytes : 0ull);
+  fa::TopkProblem p;
+  p.scores = scores;
+  p.row_stride = row_stride;
+  p.B = B;
+  p.V = V;
+  p.K = K;
+  p.chunk = t.chunk;
+  p.n_chunks = t.n_chunks;
+  p.cand = static_cast<uint64_t*>(workspace);
+  p.values = values;
+  p.indices = indices;
+  err = fa::launch_topk(p, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "top-K kernel launch");
+  return FA_OK;
+}
 
 fa_status_t fa_mha_kv_cache_plan(int B, int Sq, int S_cache, int H, int Hkv, int D, int mask_kind,
                                  int local_window_size, int num_splits, int num_sms,

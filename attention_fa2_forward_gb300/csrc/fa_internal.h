@@ -76,6 +76,22 @@ cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, co
 cudaError_t launch_fwd_f32_simt(const FwdProblem& p, float* out, const float* q, const float* k,
                                 const float* v, cudaStream_t stream);
 
+// Exact top-K per row (values descending in IEEE total order, ties by
+// ascending index): chunk kernel (grid n_chunks x B) writing each chunk's top
+// K keys to `cand` [B, n_chunks, K], then a merge kernel per row.
+constexpr int kMaxTopK = 1024;
+constexpr int kMaxTopkCandidates = 16384;  // n_chunks * K, the merge's shared memory
+struct TopkProblem {
+  const float* scores;   // [B, V] fp32, row_stride elements apart
+  long long row_stride;
+  int B, V, K;
+  int chunk, n_chunks;   // elements per chunk (multiple of 1024), chunks per row
+  uint64_t* cand;        // workspace: B * n_chunks * K keys
+  float* values;         // [B, K]
+  int* indices;          // [B, K]
+};
+cudaError_t launch_topk(const TopkProblem& p, cudaStream_t stream);
+
 // Stores `msg` as the calling thread's fa_last_error_message().
 void record_error_message(const char* msg);
 

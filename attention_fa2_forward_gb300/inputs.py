@@ -154,3 +154,33 @@ def make_kv_cache(B: int, Sq: int, S_cache: int, H: int, Hkv: int, D: int, seed:
 
 def kv_workload_inputs(w: KvWorkload):
     return make_kv_cache(w.B, w.Sq, w.S_cache, w.H, w.Hkv, w.D, w.seed, ragged=w.ragged)
+
+
+# ---------------------------------------------------------------- top-K
+
+@dataclass(frozen=True)
+class TopkWorkload:
+    """Top-K selection over B rows of V fp32 scores (next-token logits)."""
+    name: str
+    B: int
+    V: int
+    K: int
+    seed: int = 3000
+
+    def describe(self) -> str:
+        return f"B{self.B} V{self.V} K{self.K} fp32"
+
+
+TOPK_WORKLOADS = {
+    # A batch of next-token logits over a 128k vocabulary, top 50.
+    "topk_b64_v131072_k50": TopkWorkload("topk_b64_v131072_k50", 64, 131072, 50, seed=3001),
+    # 256 rows over a 256k vocabulary (268 MB of logits, more than L2), top 50.
+    "topk_b256_v262144_k50": TopkWorkload("topk_b256_v262144_k50", 256, 262144, 50, seed=3002),
+}
+
+
+def make_scores(B: int, V: int, seed: int) -> torch.Tensor:
+    """CPU fp32 scores [B, V] drawn N(0, 1) with a seeded generator."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return torch.randn((B, V), generator=g, dtype=torch.float32)

@@ -623,6 +623,152 @@ def bench_kv_ours(args, w, world, rank, local, dist):
     }
 
 
+TOPK_METRIC = "top-K selection HBM GB/s (algorithmic bytes: scores read once, values and indices written)"
+
+
+def topk_bytes(w) -> int:
+    return w.B * w.V * 4 + w.B * w.K * 8
+
+
+def bench_topk_reference(args, w, world, rank):
+    """The numpy top-K oracle on the host cores, on the first rows of the
+    workload."""
+    if rank != 0:
+        return None
+    from attention_fa2_forward_gb300.inputs import make_scores
+    from oracle import topk as topk_oracle
+    scores = make_scores(w.B, w.V, w.seed).numpy()
+    rows = max(1, min(w.B, 16))
+
+    def one():
+        t0 = time.perf_counter()
+        topk_oracle.topk(scores[:rows], w.K)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        one()
+    times = [one() for _ in range(args.steps)]
+    byts = rows * w.V * 4 + rows * w.K * 8
+    value = byts * args.steps / sum(times) / 1e9
+    sample = f"rows 0..{rows - 1} of {w.B}: {byts / 1e6:.1f} MB per step"
+    return {
+        "impl": "reference", "metric": TOPK_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sum(times) / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.describe(), "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def bench_topk_ours(args, w, world, rank, local, dist):
+    import torch
+
+    import attention_fa2_forward_gb300 as fa
+    from attention_fa2_forward_gb300.inputs import make_scores
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    scores_h = make_scores(w.B, w.V, w.seed)
+    scores = scores_h.to(dev)
+    values = torch.empty((w.B, w.K), dtype=torch.float32, device=dev)
+    indices = torch.empty((w.B, w.K), dtype=torch.int32, device=dev)
+    chunks, ws_bytes = fa.topk_plan(w.B, w.V, w.K)
+    ws = torch.empty(max(ws_bytes, 8), dtype=torch.uint8, device=dev)
+    big = scores.numel() * 4 > 2 * L2_BYTES
+    flush = torch.empty(0 if big else L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.topk(scores, w.K, values=values, indices=indices, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier(dist)
+    torch.cuda.synchronize()
+    clocks.start()
+    for s in range(args.steps):
+        flush.zero_()
+        torch.cuda._sleep(SPIN_CYCLES)
+        starts[s].record(stream)
+        step()
+        ends[s].record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    barrier(dist)
+    local_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
+    total_ms = max_over_ranks(local_ms, dist)
+    byts = topk_bytes(w)
+    ms_per_step = total_ms / args.steps
+    value = world * byts / (ms_per_step * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        sp = scores_h.pin_memory()
+        vp = torch.empty(values.shape, dtype=values.dtype, pin_memory=True)
+        ip = torch.empty(indices.shape, dtype=indices.dtype, pin_memory=True)
+        e2e_steps = max(1, min(args.steps, 20))
+
+        def e2e_step():
+            scores.copy_(sp, non_blocking=True)
+            step()
+            vp.copy_(values, non_blocking=True)
+            ip.copy_(indices, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist) / e2e_steps
+        e2e = {"value": world * byts / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": sp.numel() * 4,
+               "d2h_bytes_per_step": vp.numel() * 4 + ip.numel() * 4, "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = bench_topk_reference(argparse.Namespace(steps=1, warmup=0), w, 1, 0)["cpu_baseline"]
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = byts / (local_ms / args.steps * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": profiled_traffic(w.name, "topk_chunk_kernel", "topk.cu"),
+                "peak_source": f"{peak_src} (HBM copy, MEASURED_PEAKS.json)"
+                if peak_src == "measured" else "fallback",
+                "algorithmic_bytes": byts}
+    return {
+        "metric": TOPK_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.describe(), "B": w.B, "V": w.V, "K": w.K,
+                   "chunks_per_row": chunks, "bytes_per_step": byts,
+                   "l2": (f"no flush: the step reads {scores.numel() * 4 / 1e6:.0f} MB, more "
+                          f"than the {L2_BYTES / 1e6:.0f} MB L2") if big
+                   else "flushed (256 MiB write) before every step",
+                   "timing": "CUDA events around each step; a GPU spin before the start event "
+                             "hides host launch latency (e2e includes it)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": clocks.summary(), "gpu_launches": args.steps * 2,
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -639,20 +785,24 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
-    from attention_fa2_forward_gb300.inputs import KV_WORKLOADS, WORKLOADS
-    kv = args.workload in KV_WORKLOADS
-    if not kv and args.workload not in WORKLOADS:
-        ap.error(f"unknown workload {args.workload!r} "
-                 f"(choose from {sorted(WORKLOADS) + sorted(KV_WORKLOADS)})")
-    w = KV_WORKLOADS[args.workload] if kv else WORKLOADS[args.workload]
+    from attention_fa2_forward_gb300.inputs import KV_WORKLOADS, TOPK_WORKLOADS, WORKLOADS
+    arms = {}
+    for table, ref, ours in ((WORKLOADS, bench_reference, bench_ours),
+                             (KV_WORKLOADS, bench_kv_reference, bench_kv_ours),
+                             (TOPK_WORKLOADS, bench_topk_reference, bench_topk_ours)):
+        for name, wl in table.items():
+            arms[name] = (wl, ref, ours)
+    if args.workload not in arms:
+        ap.error(f"unknown workload {args.workload!r} (choose from {sorted(arms)})")
+    w, ref_arm, our_arm = arms[args.workload]
     world, rank, local = dist_env()
     if args.impl == "reference":
-        res = (bench_kv_reference if kv else bench_reference)(args, w, world, rank)
+        res = ref_arm(args, w, world, rank)
         if res is not None:
             print(json.dumps(res), flush=True)
         return 0
     dist = init_dist(world, "nccl")
-    res = (bench_kv_ours if kv else bench_ours)(args, w, world, rank, local, dist)
+    res = our_arm(args, w, world, rank, local, dist)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if dist is not None:

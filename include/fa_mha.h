@@ -190,6 +190,35 @@ fa_status_t fa_mha_kv_cache_plan(int B, int Sq, int S_cache, int H, int Hkv, int
                                  int *splits_out, unsigned long long *workspace_bytes_out);
 
 /*
+ * fa_topk -- exact top-K selection per row: the op of the Modular recipe
+ * "Custom Operations: Applications in AI Models", section "Optimizing top-K
+ * token sampling for GPUs in MAX" (each row of scores comes back ordered by
+ * highest value, as values and indices). Order: descending IEEE-754 total
+ * order (-NaN < -inf < ... < -0 < +0 < ... < +inf < +NaN); equal values by
+ * ascending index, so the result is unique.
+ *
+ *   values  : device, [B, K] fp32, written (descending).
+ *   indices : device, [B, K] int32, written (column of each value in its row).
+ *   scores  : device, [B, V] fp32, rows row_stride elements apart (>= V).
+ *   B, V, K : 1 <= B <= 65535, V >= 1, 1 <= K <= min(V, 1024).
+ *   workspace, workspace_bytes : caller-owned device scratch of at least the
+ *             size fa_topk_plan returns for (B, V, K); 8-byte aligned.
+ *   stream  : cudaStream_t as void*.
+ * Asynchronous; argument errors are returned before any CUDA call.
+ */
+fa_status_t fa_topk(float *values, int *indices, const float *scores, int B, int V,
+                    long long row_stride, int K, void *workspace,
+                    unsigned long long workspace_bytes, void *stream);
+
+/*
+ * fa_topk_plan -- chunks per row and workspace bytes fa_topk uses for (B, V,
+ * K); num_sms = 0 plans for the current device, n >= 1 for an n-SM device
+ * (no CUDA call).
+ */
+fa_status_t fa_topk_plan(int B, int V, int K, int num_sms, int *chunks_out,
+                         unsigned long long *workspace_bytes_out);
+
+/*
  * fa_device_status -- synchronises `device` (cudaDeviceSynchronize) and reads
  * its sticky status word: FA_OK, or FA_ERR_TIMEOUT if any kernel since the
  * last clear abandoned a bounded wait. With clear != 0 the word is reset.

@@ -1,0 +1,101 @@
+"""GPU parity of fa_topk (through the C ABI) against the CPU top-K oracle:
+values and indices must match bit for bit (the order is total, so the answer
+is unique)."""
+import struct
+
+import numpy as np
+import pytest
+import torch
+
+import attention_fa2_forward_gb300 as fa
+from attention_fa2_forward_gb300.inputs import TOPK_WORKLOADS, make_scores
+from oracle import topk as topk_oracle
+
+pytestmark = pytest.mark.gpu
+
+NEG_NAN = struct.unpack("<f", struct.pack("<I", 0xffc00000))[0]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    fa.build()
+    fa.load_library()
+    yield
+    assert fa.device_status() == fa.FA_OK
+
+
+def _check(scores_cpu, k, scores_dev=None):
+    x = scores_cpu.numpy()
+    dev = scores_dev if scores_dev is not None else scores_cpu.cuda()
+    vals, idx = fa.topk(dev, k)
+    torch.cuda.synchronize()
+    ref_v, ref_i = topk_oracle.topk(x, k)
+    got_i = idx.cpu().numpy()
+    got_v = vals.cpu().numpy()
+    np.testing.assert_array_equal(got_i, ref_i)
+    assert got_v.tobytes() == ref_v.tobytes(), "values differ bit-wise"
+
+
+@pytest.mark.parametrize("k", [1, 7, 50, 128, 1000, 1024])
+@pytest.mark.parametrize("V", [1024, 5000, 40003])
+def test_random_rows(k, V):
+    if k > V:
+        pytest.skip("k > V")
+    _check(make_scores(5, V, 100 + V + k), k)
+
+
+@pytest.mark.parametrize("k", [1, 3, 64, 500])
+def test_many_ties(k):
+    g = torch.Generator().manual_seed(7)
+    x = torch.randint(-3, 4, (4, 9000), generator=g).float()
+    _check(x, k)
+
+
+def test_all_equal_rows_take_the_lowest_indices():
+    _check(torch.full((3, 7000), 2.5), 100)
+
+
+def test_specials_signed_zeros_infinities_nans():
+    g = torch.Generator().manual_seed(8)
+    x = torch.randn((4, 3000), generator=g)
+    x[0, 10] = float("inf")
+    x[0, 20] = float("-inf")
+    x[1, 5] = float("nan")
+    x[1, 6] = NEG_NAN
+    x[2, :] = 0.0
+    x[2, ::3] = -0.0
+    x[3, 100:200] = float("inf")
+    _check(x, 150)
+
+
+@pytest.mark.parametrize("order", ["ascending", "descending"])
+def test_sorted_rows(order):
+    """Ascending rows make every element beat the running threshold (a prune
+    every step); descending rows settle the threshold at once."""
+    v = torch.arange(20000, dtype=torch.float32) * 0.01
+    if order == "descending":
+        v = v.flip(0)
+    _check(torch.stack([v, -v]), 333)
+
+
+def test_short_rows_and_k_equal_v():
+    for V in (1, 2, 5, 17, 1023):
+        x = make_scores(3, V, V)
+        _check(x, V)
+        _check(x, 1)
+
+
+def test_strided_rows():
+    wide = make_scores(6, 9000, 9)
+    x = wide[:, 100:8100]
+    dev = wide.cuda()[:, 100:8100]
+    assert dev.stride(0) == 9000
+    _check(x.contiguous(), 77, dev)
+
+
+@pytest.mark.parametrize("name", sorted(TOPK_WORKLOADS))
+def test_topk_workload_full_size(name):
+    w = TOPK_WORKLOADS[name]
+    _check(make_scores(w.B, w.V, w.seed), w.K)
