@@ -38,6 +38,7 @@ FA_ERR_TIMEOUT = 4
 
 # Every symbol the header declares (checked by the tests).
 EXPORTS = ("fa_mha_no_cache", "fa_mha_no_cache_strided", "fa_mha_no_cache_noalloc",
+           "fa_mha_no_cache_f32_tc", "fa_mha_no_cache_f32_tc_workspace",
            "fa_mha_kv_cache", "fa_mha_kv_cache_plan", "fa_topk", "fa_topk_plan",
            "fa_device_status",
            "fa_set_wait_timeout_ns", "fa_set_stall_probe", "fa_status_string",
@@ -80,6 +81,11 @@ def load_library(path: str | None = None):
         lib.fa_mha_kv_cache_plan.restype = i
         lib.fa_mha_kv_cache_plan.argtypes = [i, i, i, i, i, i, i, i, i, i,
                                              ctypes.POINTER(i), ctypes.POINTER(ull)]
+        lib.fa_mha_no_cache_f32_tc.restype = i
+        lib.fa_mha_no_cache_f32_tc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float,
+                                               i, i, vp, ull, vp]
+        lib.fa_mha_no_cache_f32_tc_workspace.restype = ull
+        lib.fa_mha_no_cache_f32_tc_workspace.argtypes = [i, i, i, i]
         lib.fa_topk.restype = i
         lib.fa_topk.argtypes = [vp, vp, vp, i, i, ctypes.c_longlong, i, vp, ull, vp]
         lib.fa_topk_plan.restype = i
@@ -135,7 +141,8 @@ def _dtype_code(dt: torch.dtype) -> int:
 def mha_no_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float | None = None,
                  mask="causal", window: int = -1, *, out: torch.Tensor | None = None,
                  lse: torch.Tensor | None = None, return_lse: bool = False,
-                 stream: torch.cuda.Stream | None = None):
+                 stream: torch.cuda.Stream | None = None, fp32_tensor_cores: bool = True,
+                 workspace: torch.Tensor | None = None):
     """Fused attention forward (``mo.mha.no_cache``) on the current CUDA device.
 
     q: [B, S, H, D]; k, v: [B, S, Hkv, D]; CUDA tensors of one dtype (bf16 or
@@ -144,7 +151,10 @@ def mha_no_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float
     "none" or "causal"; ``window`` > 0 adds a sliding window (causal: the W
     keys ending at the query; none: keys within W - 1 on either side).
     Returns out [B, S, H, D] (q's dtype), and lse [B, H, S] fp32 if
-    ``return_lse``; a given ``out`` may also be a strided view.
+    ``return_lse``; a given ``out`` may also be a strided view. fp32 tensors
+    run on the tensor cores (three bf16 parts per value, fp32 accuracy) when
+    they are dense with D in {64, 128} and ``fp32_tensor_cores``; otherwise on
+    the CUDA-core fp32 kernel.
     """
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D (BSHD)")
@@ -179,7 +189,16 @@ def mha_no_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float
     with torch.cuda.device(q.device):
         st = stream if stream is not None else torch.cuda.current_stream(q.device)
         lse_ptr = lse.data_ptr() if lse is not None else None
-        if all(t.is_contiguous() for t in (q, k, v, out)):
+        dense = all(t.is_contiguous() for t in (q, k, v, out))
+        if dtype == DTYPE_F32 and fp32_tensor_cores and dense and D in (64, 128):
+            ws_bytes = int(lib.fa_mha_no_cache_f32_tc_workspace(B, S, Hkv, D))
+            if workspace is None or workspace.numel() * workspace.element_size() < ws_bytes:
+                workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+            rc = lib.fa_mha_no_cache_f32_tc(
+                out.data_ptr(), lse_ptr, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                B, S, H, Hkv, D, float(scale), _mask_code(mask), int(window),
+                workspace.data_ptr(), ws_bytes, st.cuda_stream)
+        elif dense:
             rc = lib.fa_mha_no_cache(
                 out.data_ptr(), lse_ptr, q.data_ptr(), k.data_ptr(), v.data_ptr(),
                 B, S, H, Hkv, D, float(scale), _mask_code(mask), int(window), dtype,

@@ -441,6 +441,73 @@ fa_status_t fa_topk(float* values, int* indices, const float* scores, int B, int
   return FA_OK;
 }
 
+unsigned long long fa_mha_no_cache_f32_tc_workspace(int B, int S, int Hkv, int D) {
+  if (B < 1 || S < 1 || Hkv < 1 || (D != 64 && D != 128)) return 0ull;
+  return fa::f32x3_workspace_bytes(B, S, Hkv, D);
+}
+
+fa_status_t fa_mha_no_cache_f32_tc(float* out, float* lse, const float* q, const float* k,
+                                   const float* v, int B, int S, int H, int Hkv, int D, float scale,
+                                   int mask_kind, int local_window_size, void* workspace,
+                                   unsigned long long workspace_bytes, void* stream) {
+  if (out == nullptr || q == nullptr || k == nullptr || v == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "null tensor pointer");
+  if (B < 1 || S < 1 || H < 1 || Hkv < 1)
+    return fail(FA_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d S=%d H=%d Hkv=%d)", B, S, H, Hkv);
+  if (H % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "H=%d is not a multiple of Hkv=%d", H, Hkv);
+  if (mask_kind != FA_MASK_NONE && mask_kind != FA_MASK_CAUSAL)
+    return fail(FA_ERR_INVALID_ARG, "unknown mask kind %d", mask_kind);
+  if (local_window_size == 0 || local_window_size < -1)
+    return fail(FA_ERR_INVALID_ARG, "local_window_size must be -1 or >= 1 (got %d)",
+                local_window_size);
+  if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARG, "scale must be finite");
+  if (scale < 0.f) return fail(FA_ERR_UNSUPPORTED, "negative scale is not supported");
+  if (D != 64 && D != 128) return fail(FA_ERR_UNSUPPORTED, "head dim D=%d (64 or 128)", D);
+  const long long elems_q = static_cast<long long>(B) * S * H * D;
+  if (elems_q >= (1ll << 40) || static_cast<long long>(S) * H * D * 4 >= (1ll << 39) ||
+      static_cast<long long>(B) * H * ((S + 127) / 128) > 0x7fffffffll)
+    return fail(FA_ERR_UNSUPPORTED, "problem too large");
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      (lse != nullptr && !aligned(lse, 4)) || (workspace != nullptr && !aligned(workspace, 256)))
+    return fail(FA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned (workspace 256)");
+  const unsigned long long need = fa::f32x3_workspace_bytes(B, S, Hkv, D);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(FA_ERR_INVALID_ARG, "workspace of %llu bytes needed, %llu given", need,
+                workspace != nullptr ? workspace_bytes : 0ull);
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(FA_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+  unsigned* status = nullptr;
+  fa_status_t st = device_status_word(dev, &status);
+  if (st != FA_OK) return st;
+  fa::F32x3Problem p{};
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.causal = mask_kind == FA_MASK_CAUSAL ? 1 : 0;
+  p.window = local_window_size > 0 && local_window_size < S ? local_window_size : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.lse = lse;
+  p.status = status;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.stall_probe = g_stall_probe.load();
+  err = fa::launch_fwd_f32x3_tc(p, workspace, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "fp32 tensor-core kernel launch");
+  return FA_OK;
+}
+
 fa_status_t fa_mha_kv_cache_plan(int B, int Sq, int S_cache, int H, int Hkv, int D, int mask_kind,
                                  int local_window_size, int num_splits, int num_sms,
                                  int* splits_out, unsigned long long* workspace_bytes_out) {

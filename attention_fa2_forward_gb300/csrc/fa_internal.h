@@ -76,6 +76,29 @@ cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, co
 cudaError_t launch_fwd_f32_simt(const FwdProblem& p, float* out, const float* q, const float* k,
                                 const float* v, cudaStream_t stream);
 
+// fp32 forward on the tensor cores: every operand split into three bf16
+// parts, six part products per contraction. q/out dense or strided BSHD
+// (sq/so, zero: dense); k/v dense [B, S, Hkv, D], split into bf16 planes in
+// a workspace of f32x3_workspace_bytes() bytes.
+struct F32x3Problem {
+  int B, S, H, Hkv, D;
+  int causal, window;
+  float scale, scale_log2;
+  const float* q;
+  const float* k;
+  const float* v;
+  float* out;
+  float* lse;            // [B, H, S] or nullptr
+  uint16_t* kp[3];       // K's bf16 planes (set by the launcher from the workspace)
+  uint16_t* vp[3];       // V's bf16 planes
+  BshdStrides sq, so;
+  unsigned* status;
+  unsigned long long wait_limit_ns;
+  int stall_probe;
+};
+unsigned long long f32x3_workspace_bytes(int B, int S, int Hkv, int D);
+cudaError_t launch_fwd_f32x3_tc(F32x3Problem p, void* workspace, cudaStream_t stream);
+
 // Exact top-K per row (values descending in IEEE total order, ties by
 // ascending index): chunk kernel (grid n_chunks x B) writing each chunk's top
 // K keys to `cand` [B, n_chunks, K], then a merge kernel per row.

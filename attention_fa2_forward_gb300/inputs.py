@@ -59,6 +59,9 @@ WORKLOADS = {
     # Other head dims: 96 (padded to the 128-column kernel), 256 (one-Q-tile kernel).
     "gqa_s4096_d96": Workload("gqa_s4096_d96", 2, 4096, 32, 8, 96, "bf16", True, seed=1005),
     "gqa_s4096_d256": Workload("gqa_s4096_d256", 2, 4096, 16, 8, 256, "bf16", True, seed=1006),
+    # fp32 inputs on the tensor cores (three bf16 parts per value).
+    "gqa_s4096_d128_f32": Workload("gqa_s4096_d128_f32", 2, 4096, 32, 8, 128, "f32", True,
+                                   seed=1007),
 }
 
 

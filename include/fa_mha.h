@@ -140,6 +140,32 @@ fa_status_t fa_mha_no_cache_noalloc(void *out, float *lse, const void *q, const 
                                     void *stream, int check_status);
 
 /*
+ * fa_mha_no_cache_f32_tc -- fa_mha_no_cache for fp32 tensors on the tensor
+ * cores at fp32 accuracy (the page's `scale: Float32` interface with fp32
+ * q, k, v): every operand is split into three bf16 parts (x = b0 + b1 + b2,
+ * 24 significant bits) and each contraction sums the six part products down
+ * to 2^-16 of the leading one, with fp32 accumulation; max-abs error on the
+ * bench workloads stays within 1e-4 of the exact result, like the CUDA-core
+ * fp32 path (FA_DTYPE_F32 of fa_mha_no_cache).
+ *
+ *   out, lse, q, k, v, sizes, scale, mask_kind, local_window_size : as
+ *             fa_mha_no_cache with fp32 data, dense BSHD / BShD, 16-byte
+ *             aligned; D in {64, 128}; finite inputs.
+ *   workspace, workspace_bytes : caller-owned device scratch of at least
+ *             fa_mha_no_cache_f32_tc_workspace(B, S, Hkv, D) bytes (K's and
+ *             V's bf16 planes), 256-byte aligned.
+ * Asynchronous on `stream`; errors as fa_mha_no_cache.
+ */
+fa_status_t fa_mha_no_cache_f32_tc(float *out, float *lse, const float *q, const float *k,
+                                   const float *v, int B, int S, int H, int Hkv, int D,
+                                   float scale, int mask_kind, int local_window_size,
+                                   void *workspace, unsigned long long workspace_bytes,
+                                   void *stream);
+
+/* Bytes of workspace fa_mha_no_cache_f32_tc needs (0 for unsupported sizes). */
+unsigned long long fa_mha_no_cache_f32_tc_workspace(int B, int S, int Hkv, int D);
+
+/*
  * fa_mha_kv_cache -- attention over a KV cache (bf16, tensor cores). The
  * pages document only the no-cache operator; this is its cached sibling read
  * the plain way: the same operator (FlashAttentionGPU.execute, Steps -1 to 4)

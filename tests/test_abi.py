@@ -109,3 +109,32 @@ def _call_strided(lib, strides=((64, 32, 16),) * 4, q=P, dtype=0, null=None):
 def test_strided_validation_happens_before_cuda(lib, kw, code):
     assert _call_strided(lib, **kw) == code
     assert lib.fa_last_error_message()
+
+
+def _call_f32tc(lib, out=P, q=P, k=P, v=P, B=1, S=8, H=2, Hkv=2, D=64, scale=0.125, mask=1,
+                window=-1, ws=P, ws_bytes=1 << 30):
+    return lib.fa_mha_no_cache_f32_tc(out, None, q, k, v, B, S, H, Hkv, D, scale, mask, window, ws,
+                                      ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=3, Hkv=2), fa.FA_ERR_INVALID_ARG),
+    (dict(window=0), fa.FA_ERR_INVALID_ARG),
+    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(q=P + 4), fa.FA_ERR_UNSUPPORTED),
+    (dict(ws=P + 16), fa.FA_ERR_UNSUPPORTED),
+    (dict(ws_bytes=16), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=None), fa.FA_ERR_INVALID_ARG),
+])
+def test_f32_tensor_core_validation_happens_before_cuda(lib, kw, code):
+    assert _call_f32tc(lib, **kw) == code
+    assert lib.fa_last_error_message()
+
+
+def test_f32_tensor_core_workspace_size(lib):
+    # six bf16 planes of [B, S, Hkv, D] (K's and V's three parts), 256-byte rounded
+    plane = 2 * 100 * 4 * 128 * 2
+    assert lib.fa_mha_no_cache_f32_tc_workspace(2, 100, 4, 128) == 6 * (-(-plane // 256) * 256)
+    assert lib.fa_mha_no_cache_f32_tc_workspace(2, 100, 4, 96) == 0

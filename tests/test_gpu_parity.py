@@ -32,7 +32,7 @@ def _built():
     assert fa.device_status() == fa.FA_OK
 
 
-def _run_gpu(q, k, v, scale, causal, window, poison=True):
+def _run_gpu(q, k, v, scale, causal, window, poison=True, fp32_tensor_cores=True):
     dev = torch.device("cuda:0")
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     out = torch.empty_like(qd)
@@ -41,7 +41,8 @@ def _run_gpu(q, k, v, scale, causal, window, poison=True):
     if poison:
         out.fill_(float("nan"))
         lse.fill_(float("nan"))
-    fa.mha_no_cache(qd, kd, vd, scale, "causal" if causal else "none", window, out=out, lse=lse)
+    fa.mha_no_cache(qd, kd, vd, scale, "causal" if causal else "none", window, out=out, lse=lse,
+                    fp32_tensor_cores=fp32_tensor_cores)
     torch.cuda.synchronize()
     return out.double().cpu().numpy(), lse.double().cpu().numpy()
 
@@ -62,10 +63,10 @@ def _compare(out, lse, ref_out, ref_lse, dtype, label):
 
 
 def _full_case(oracle_mod, B, S, H, Hkv, D, dtype, causal, window, seed, scale=None,
-               q_std=1.0, k_std=1.0, v_dist="normal"):
+               q_std=1.0, k_std=1.0, v_dist="normal", fp32_tensor_cores=True):
     q, k, v = make_qkv(B, S, H, Hkv, D, dtype, seed, q_std=q_std, k_std=k_std, v_dist=v_dist)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
-    out, lse = _run_gpu(q, k, v, scale, causal, window)
+    out, lse = _run_gpu(q, k, v, scale, causal, window, fp32_tensor_cores=fp32_tensor_cores)
     ref_out, ref_lse = oracle_mod.mha_forward(q, k, v, scale, causal, window)
     label = f"B{B} S{S} H{H}/{Hkv} D{D} {dtype} causal={causal} W={window}"
     return _compare(out, lse, ref_out, ref_lse, dtype, label)
@@ -101,7 +102,7 @@ def _sample_rows(S, seed, n_random=40):
 
 
 @pytest.mark.parametrize("name", ["gqa_s4096_d128", "swa_s16384_w4096", "mqa_s32768_stress",
-                                  "gqa_s4096_d96", "gqa_s4096_d256"])
+                                  "gqa_s4096_d96", "gqa_s4096_d256", "gqa_s4096_d128_f32"])
 def test_full_size_workload_sampled_rows(oracle_mod, name):
     w = WORKLOADS[name]
     q, k, v = workload_inputs(w)
@@ -109,7 +110,7 @@ def test_full_size_workload_sampled_rows(oracle_mod, name):
     rows = _sample_rows(w.S, w.seed)
     ref_out, ref_lse = oracle_mod.mha_forward(q[:, rows], k, v, w.scale, w.causal, w.window,
                                               rows=rows)
-    _compare(out[:, rows], lse[:, :, rows], ref_out, ref_lse, torch.bfloat16, name)
+    _compare(out[:, rows], lse[:, :, rows], ref_out, ref_lse, w.torch_dtype, name)
     # Every element was written (the buffers were NaN-poisoned).
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
@@ -178,6 +179,29 @@ def test_other_head_dims_long_sampled_rows(oracle_mod, D, H, Hkv, window):
     _compare(out[:, rows], lse[:, :, rows], ref_out, ref_lse, torch.bfloat16,
              f"S4100 D{D} W{window}")
     assert np.isfinite(out).all()
+
+
+# fp32: dense D = 64 / 128 runs on the tensor cores (three bf16 parts per value) by
+# default; these cases pin the CUDA-core fp32 kernel as well, and the tensor-core
+# path on longer sequences and large logits at the same 1e-4 bound.
+@pytest.mark.parametrize("S,H,Hkv,D,causal,window", [
+    (129, 2, 1, 64, True, -1), (300, 4, 2, 128, False, -1), (513, 2, 2, 128, True, 100),
+    (700, 4, 1, 64, False, 200)])
+def test_fp32_cuda_core_path(oracle_mod, S, H, Hkv, D, causal, window):
+    _full_case(oracle_mod, 2, S, H, Hkv, D, torch.float32, causal, window, seed=70 + S,
+               fp32_tensor_cores=False)
+
+
+@pytest.mark.parametrize("S,H,Hkv,D,causal,window", [
+    (1000, 4, 2, 128, True, -1), (2049, 2, 1, 64, True, -1), (1500, 4, 4, 128, False, -1),
+    (1800, 4, 2, 128, True, 300), (1000, 2, 2, 64, False, 150)])
+def test_fp32_tensor_core_path(oracle_mod, S, H, Hkv, D, causal, window):
+    _full_case(oracle_mod, 1, S, H, Hkv, D, torch.float32, causal, window, seed=80 + S)
+
+
+def test_fp32_tensor_core_path_large_logits(oracle_mod):
+    _full_case(oracle_mod, 1, 1100, 4, 1, 128, torch.float32, True, -1, seed=91, q_std=3.0,
+               k_std=3.0, v_dist="uniform")
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
