@@ -360,7 +360,9 @@ struct TopkPlan {
 // candidates per row for the merge.
 TopkPlan make_topk_plan(int B, int V, int K, int num_sms) {
   constexpr long long kStep = 2048;
-  long long chunks = (2ll * num_sms + B - 1) / B;
+  // At most one wave of chunk CTAs (two resident per SM): a second, partial
+  // wave would take as long as a full one.
+  long long chunks = 2ll * num_sms / B;
   const long long by_merge = 4096 / K > 0 ? 4096 / K : 1;
   if (chunks > by_merge) chunks = by_merge;
   if (chunks < 1) chunks = 1;
@@ -369,7 +371,9 @@ TopkPlan make_topk_plan(int B, int V, int K, int num_sms) {
   TopkPlan t;
   t.chunk = static_cast<int>(chunk);
   t.n_chunks = static_cast<int>((V + chunk - 1) / chunk);
-  t.workspace_bytes = static_cast<unsigned long long>(B) * t.n_chunks * K * 8ull;
+  // A row of one chunk is finished by its chunk CTA: no candidates to keep.
+  t.workspace_bytes =
+      t.n_chunks == 1 ? 0ull : static_cast<unsigned long long>(B) * t.n_chunks * K * 8ull;
   return t;
 }
 
@@ -422,7 +426,7 @@ fa_status_t fa_topk(float* values, int* indices, const float* scores, int B, int
     return fail(FA_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
   if ((st = current_sm_count(&sms)) != FA_OK) return st;
   const TopkPlan t = make_topk_plan(B, V, K, sms);
-  if (workspace == nullptr || workspace_bytes < t.workspace_bytes)
+  if (t.workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < t.workspace_bytes))
     return fail(FA_ERR_INVALID_ARG, "workspace of %llu bytes needed, %llu given",
                 t.workspace_bytes, workspace != nullptr ? workspace_bytes : 0ull);
   fa::TopkProblem p;

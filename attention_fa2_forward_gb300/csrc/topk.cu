@@ -16,7 +16,10 @@
 //     CTA streams one contiguous front of memory) without block barriers (8
 //     elements per lane per step, staged by asynchronous 16-byte copies (4-byte
 //     when the rows are not 16-byte aligned) in a shared-memory ring with
-//     seven steps in flight). A
+//     seven steps in flight). Before the scan the CTA seeds its threshold
+//     from the first four staged steps: the K-th largest of the per-lane,
+//     per-step maxima (1024 distinct elements), rounded down, is a lower
+//     bound of the chunk's K-th key. A
 //     warp keeps only keys above the best threshold any warp of the CTA has
 //     published (the value half of the key is compared first), each lane
 //     appending its own rare candidates to a warp-private buffer;
@@ -25,10 +28,13 @@
 //     soon as the bucket holding the K-th key holds exactly the keys still
 //     needed; warp-private histogram) and publishes its K-th key (the
 //     smallest survivor) as a threshold for the whole CTA. At the end the CTA selects the top K of its warps'
-//     survivors once (block-wide) and writes them (padded with key 0, below
-//     every real key, when the chunk is shorter) to the workspace;
-//   * merge kernel: one CTA per row selects the top K of the chunks'
-//     candidates the same way and sorts them (bitonic, descending).
+//     survivors once (block-wide). A chunk that is the whole row writes
+//     them sorted straight to the output; otherwise they go (padded with key
+//     0, below every real key, when the chunk is shorter) to the workspace;
+//   * merge kernel (rows of several chunks only): one CTA per row selects
+//     the top K of the chunks' candidates the same way.
+// Sorting K distinct keys: up to 128 each key's place is its count of
+// larger keys, above that a bitonic sort.
 // Scores are handled as raw 32-bit patterns from load to store: no float
 // operation touches them, so NaN payloads and signed zeros survive.
 #include <cuda_runtime.h>
@@ -272,14 +278,15 @@ __device__ __forceinline__ int step_index(int base, int e) {
 struct WarpScan {
   uint64_t* buf;
   unsigned* hist;
-  int n, prune_at;
+  int n, prune_at;           // key count (warp-uniform) and the prune trigger
   uint64_t thr;
   unsigned long long* best;  // the CTA's best threshold (shared memory)
-  int* count;                // the warp's key count (shared memory; n mirrors it)
+  uint64_t best_seen;        // its value read one step ahead
 };
 
-__device__ __forceinline__ void filter_step(const uint32_t (&x)[kPerThread], int base, int end,
-                                            int K, WarpScan& ws) {
+__device__ __forceinline__ void filter_step(const uint32_t (&x)[kPerThread],
+                                            const uint32_t* words, int base, int end, int K,
+                                            WarpScan& ws) {
   const int lane = threadIdx.x & 31;
   // Common path, 4 integer operations per element: the value half of the key
   // as a signed integer in total order (b ^ ((b >> 31) & 0x7fffffff)) against
@@ -287,9 +294,10 @@ __device__ __forceinline__ void filter_step(const uint32_t (&x)[kPerThread], int
   // pass get the exact 64-bit test below. Only a chunk's last blocks need the
   // bounds test.
   // Any warp's K-th key is a lower bound of the CTA's K-th key: filter
-  // against the best one published so far.
-  ws.thr = max(ws.thr, static_cast<uint64_t>(*reinterpret_cast<volatile unsigned long long*>(
-                           ws.best)));
+  // against the best one published so far, read during the previous step so
+  // that its latency stays off this step's path.
+  ws.thr = max(ws.thr, ws.best_seen);
+  ws.best_seen = *reinterpret_cast<volatile unsigned long long*>(ws.best);
   const int32_t s_thr = static_cast<int32_t>(static_cast<uint32_t>(ws.thr >> 32) ^ 0x80000000u);
   unsigned mask = 0;
   if (base + kWarpStep <= end) {
@@ -305,22 +313,31 @@ __device__ __forceinline__ void filter_step(const uint32_t (&x)[kPerThread], int
       if (step_index(base, e) < end && (v ^ ((v >> 31) & 0x7fffffff)) >= s_thr) mask |= 1u << e;
     }
   }
-  // Candidates are rare: each lane appends its own, taking slots from the
-  // warp's counter in shared memory (no per-element warp votes).
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    if ((mask >> e) & 1u) {
-      const uint64_t key = make_key(x[e], static_cast<uint32_t>(step_index(base, e)));
-      if (key > ws.thr) ws.buf[atomicAdd(ws.count, 1)] = key;
+  // Candidates are rare (the threshold starts seeded): a step without any
+  // costs one vote. Otherwise the warp takes one set bit per lane per round:
+  // the value comes back from this step's staging slot (intact until the
+  // next step), and a ballot gives each taken key its place after the warp's
+  // count (no atomics, the count stays in a register).
+  if (!__any_sync(0xffffffffu, mask != 0)) return;
+  const unsigned below = (1u << lane) - 1u;
+  do {
+    bool take = false;
+    uint64_t key = 0;
+    if (mask != 0) {
+      const int e = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const uint32_t v = words[128 * (e >> 2) + 4 * lane + (e & 3)];
+      key = make_key(v, static_cast<uint32_t>(step_index(base, e)));
+      take = key > ws.thr;
     }
-  }
-  __syncwarp();
-  ws.n = *reinterpret_cast<volatile int*>(ws.count);
+    const unsigned taken = __ballot_sync(0xffffffffu, take);
+    if (take) ws.buf[ws.n + __popc(taken & below)] = key;
+    ws.n += __popc(taken);
+  } while (__any_sync(0xffffffffu, mask != 0));
   if (ws.n > ws.prune_at) {
     __syncwarp();
     const Selection sel = warp_select_top(ws.buf, ws.n, K, ws.hist);
     ws.n = warp_compact(ws.buf, ws.n, sel);
-    if (lane == 0) *ws.count = ws.n;
     __syncwarp();
     // The new threshold is the exact K-th key, the smallest survivor (the
     // selection may stop at a coarse bucket; its floor would let many keys
@@ -336,10 +353,59 @@ __device__ __forceinline__ void filter_step(const uint32_t (&x)[kPerThread], int
   }
 }
 
+// Writes K distinct keys (shared memory, room for P >= K entries, P the next
+// power of two; every thread of the CTA calls this after a barrier) to one
+// output row in descending order. Up to kRankSortMax keys each key's place
+// is the number of larger keys (no barriers, K reads per key); above that a
+// bitonic sort over P entries padded with key 0.
+constexpr int kRankSortMax = 128;
+__device__ void write_sorted_row(uint64_t* keys, int K, uint32_t* values, int* indices) {
+  if (K <= kRankSortMax) {
+    for (int i = threadIdx.x; i < K; i += kThreads) {
+      const uint64_t v = keys[i];
+      int r = 0;
+      for (int j = 0; j < K; ++j) r += keys[j] > v ? 1 : 0;
+      values[r] = key_bits(v);
+      indices[r] = key_index(v);
+    }
+    return;
+  }
+  int P = 1;
+  while (P < K) P <<= 1;
+  for (int i = K + threadIdx.x; i < P; i += kThreads) keys[i] = 0ull;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P / 2; i += kThreads) {
+        const int lo = 2 * i - (i & (stride - 1));  // pairs (lo, lo + stride)
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const uint64_t a = keys[lo], c = keys[hi];
+        if ((a < c) == desc) {
+          keys[lo] = c;
+          keys[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < K; i += kThreads) {
+    values[i] = key_bits(keys[i]);
+    indices[i] = key_index(keys[i]);
+  }
+}
+
 // Dynamic shared memory of the chunk kernel: per warp a ring of kRing
 // staging slots (kWarpStep words each), a key buffer of prune_at + kWarpStep
 // keys and a 256-bin histogram, then the CTA's merge area of kWarps * K keys.
 constexpr int kRing = 8;
+constexpr int kSeedSteps = 4;  // scan steps per warp that seed the threshold
+static_assert(kSeedSteps < kRing, "the seed steps are staged by the prologue");
+static_assert(kSeedSteps * kThreads >= kMaxTopK, "at least K groups seed the threshold");
+static_assert(kSeedSteps * kThreads <= kWarps * 2 * kWarpStep, "seed keys fit the key buffers");
+constexpr int kRingKeys = kWarps * kRing * kWarpStep / 2;  // 64-bit keys the ring holds
+static_assert(kWarps * kMaxTopK <= kRingKeys, "the warps' top K always fit the idle ring");
+static_assert(kWarps >= 2, "the merge area (kWarps * K keys) holds the sort buffer");
 __host__ __device__ inline int chunk_prune_at(int K) { return K > 256 ? K : 256; }
 __host__ __device__ inline size_t chunk_smem_bytes(int K) {
   return static_cast<size_t>(kWarps) * kRing * kWarpStep * sizeof(uint32_t) +
@@ -351,12 +417,12 @@ __host__ __device__ inline size_t chunk_smem_bytes(int K) {
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads)
     topk_chunk_kernel(const float* __restrict__ scores, long long row_stride, int V, int K,
-                      int chunk, int n_chunks, uint64_t* __restrict__ cand) {
+                      int chunk, int n_chunks, uint64_t* __restrict__ cand,
+                      uint32_t* __restrict__ values, int* __restrict__ indices) {
   extern __shared__ uint64_t dyn[];
   __shared__ SelectScratch sc;
   __shared__ int s_count[kWarps];
   __shared__ unsigned long long s_best;
-  __shared__ int s_wcount[kWarps];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -389,10 +455,8 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t* row =
       reinterpret_cast<const uint32_t*>(scores) + static_cast<long long>(b) * row_stride;
   if (threadIdx.x == 0) s_best = 0ull;
-  if (lane == 0) s_wcount[warp] = 0;
   __syncthreads();
-  WarpScan ws{wbufs + warp * wcap, hists + warp * 256, 0, prune_at, 0ull, &s_best,
-              &s_wcount[warp]};
+  WarpScan ws{wbufs + warp * wcap, hists + warp * 256, 0, prune_at, 0ull, &s_best, 0ull};
 
   // kRing - 1 steps in flight: at step s the copy of step s + kRing - 1 goes
   // into the slot step s - 1 used, then the oldest copy group is awaited.
@@ -406,6 +470,48 @@ __global__ void __launch_bounds__(kThreads)
   };
 #pragma unroll
   for (int r = 0; r < kRing - 1; ++r) stage(r, r);
+
+  // Seed the CTA's threshold from the first kSeedSteps steps of every warp
+  // (already staged): per lane and step the largest of its scores, one
+  // distinct element per group, as a key whose low half is a distinct id
+  // (key 0 marks a group without elements). The value half of the K-th
+  // largest of these keys, rounded down by the radix select, is at or below
+  // at least K elements of the chunk, so it bounds the chunk's K-th key from
+  // below: nothing the top K needs is filtered out. Starting every warp near
+  // the K-th of the 8 * kSeedSteps * kThreads sampled scores instead of from
+  // zero leaves a warp with a few dozen candidates per chunk and rarely a
+  // prune.
+  cp_async_wait<kRing - 1 - kSeedSteps>();
+#pragma unroll
+  for (int s = 0; s < kSeedSteps; ++s) {
+    uint32_t x[kPerThread];
+    read_step(ring + s * kWarpStep, x);
+    int32_t best = INT_MIN;
+    bool any = false;
+    if (s < steps) {
+      const int base = block_base(s);
+#pragma unroll
+      for (int e = 0; e < kPerThread; ++e) {
+        const int32_t v = static_cast<int32_t>(x[e]);
+        if (step_index(base, e) < cend) {
+          best = max(best, v ^ ((v >> 31) & 0x7fffffff));
+          any = true;
+        }
+      }
+    }
+    const uint32_t id = static_cast<uint32_t>(s * kThreads + threadIdx.x);
+    wbufs[id] = any ? (static_cast<uint64_t>(static_cast<uint32_t>(best) ^ 0x80000000u) << 32) |
+                          (id + 1u)
+                    : 0ull;
+  }
+  __syncthreads();
+  {
+    const Selection seed = block_select_top(wbufs, kSeedSteps * kThreads, K, sc);
+    if (threadIdx.x == 0) s_best = seed.prefix & 0xffffffff00000000ull;
+  }
+  __syncthreads();  // the key buffers are reused by the scan
+  ws.thr = ws.best_seen = s_best;
+
   int slot = 0;
   for (int st = 0; st < steps; ++st) {
     const int next = slot == 0 ? kRing - 1 : slot - 1;
@@ -413,36 +519,59 @@ __global__ void __launch_bounds__(kThreads)
     cp_async_wait<kRing - 1>();
     uint32_t x[kPerThread];
     read_step(ring + slot * kWarpStep, x);
-    filter_step(x, block_base(st), cend, K, ws);  // blocks past cend are masked out
+    filter_step(x, ring + slot * kWarpStep, block_base(st), cend, K, ws);  // past cend: masked
     slot = slot == kRing - 1 ? 0 : slot + 1;
   }
   cp_async_wait<0>();
   __syncwarp();
-  if (ws.n > K) {
-    const Selection sel = warp_select_top(ws.buf, ws.n, K, ws.hist);
-    ws.n = warp_compact(ws.buf, ws.n, sel);
-  }
   if (lane == 0) s_count[warp] = ws.n;
   __syncthreads();
-  // Gather the warps' survivors (at most K each) and select the CTA's top K.
-  int off = 0, total = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < warp) off += s_count[w];
-    total += s_count[w];
+  // The warps' keys are gathered into the staging ring, idle now that every
+  // copy has landed, and the CTA selects its top K once. Only when they would
+  // not fit (large K) does each warp first cut its own keys to K.
+  int total = 0;
+  for (int w = 0; w < kWarps; ++w) total += s_count[w];
+  if (total > kRingKeys) {
+    if (ws.n > K) {
+      const Selection sel = warp_select_top(ws.buf, ws.n, K, ws.hist);
+      ws.n = warp_compact(ws.buf, ws.n, sel);
+    }
+    __syncthreads();  // every warp has read the old counts
+    if (lane == 0) s_count[warp] = ws.n;
+    __syncthreads();
+    total = 0;
+    for (int w = 0; w < kWarps; ++w) total += s_count[w];
   }
-  for (int i = lane; i < ws.n; i += 32) merged[off + i] = ws.buf[i];
+  int off = 0;
+  for (int w = 0; w < warp; ++w) off += s_count[w];
+  uint64_t* gathered = reinterpret_cast<uint64_t*>(rings);
+  for (int i = lane; i < ws.n; i += 32) gathered[off + i] = ws.buf[i];
   __syncthreads();
-  uint64_t* dst = cand + (static_cast<long long>(b) * n_chunks + c) * K;
+  // The CTA's top K go to the merge area: the keys are distinct, so exactly
+  // K match the selection (the bound only keeps a broken invariant inside
+  // the K slots).
+  uint64_t* top = merged;
   if (total > K) {
-    const Selection sel = block_select_top(merged, total, K, sc);
+    const Selection sel = block_select_top(gathered, total, K, sc);
     if (threadIdx.x == 0) sc.count = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < total; i += kThreads) {
-      const uint64_t v = merged[i];
-      if ((v & sel.mask) >= sel.prefix) dst[atomicAdd(&sc.count, 1)] = v;
+      const uint64_t v = gathered[i];
+      if ((v & sel.mask) >= sel.prefix) {
+        const int slot = atomicAdd(&sc.count, 1);
+        if (slot < K) top[slot] = v;
+      }
     }
   } else {
-    for (int i = threadIdx.x; i < K; i += kThreads) dst[i] = i < total ? merged[i] : 0ull;
+    for (int i = threadIdx.x; i < K; i += kThreads) top[i] = i < total ? gathered[i] : 0ull;
+  }
+  __syncthreads();
+  if (n_chunks == 1) {  // the chunk is the whole row: its top K is the answer
+    write_sorted_row(top, K, values + static_cast<long long>(b) * K,
+                     indices + static_cast<long long>(b) * K);
+  } else {
+    uint64_t* dst = cand + (static_cast<long long>(b) * n_chunks + c) * K;
+    for (int i = threadIdx.x; i < K; i += kThreads) dst[i] = top[i];
   }
 }
 
@@ -459,36 +588,19 @@ __global__ void __launch_bounds__(kThreads)
   // The padding keys (0) repeat, but the K largest are real and distinct:
   // every chunk contributed min(K, its length) real keys and V >= K.
   const Selection top = block_select_top(items, n, K, sc);
-  // The K winners into the sort buffer (P = next power of two >= K, padded
-  // with 0), then a bitonic sort into descending order.
-  int P = 1;
-  while (P < K) P <<= 1;
+  // The K winners into the sort buffer (room for P >= K keys after the
+  // candidates), then out in order.
   uint64_t* sel = items + n;
-  for (int i = threadIdx.x; i < P; i += kThreads) sel[i] = 0ull;
   if (threadIdx.x == 0) sc.count = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += kThreads)
-    if ((items[i] & top.mask) >= top.prefix) sel[atomicAdd(&sc.count, 1)] = items[i];
-  __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < P / 2; i += kThreads) {
-        const int lo = 2 * i - (i & (stride - 1));  // pairs (lo, lo + stride)
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const uint64_t a = sel[lo], c = sel[hi];
-        if ((a < c) == desc) {
-          sel[lo] = c;
-          sel[hi] = a;
-        }
-      }
-      __syncthreads();
+    if ((items[i] & top.mask) >= top.prefix) {
+      const int slot = atomicAdd(&sc.count, 1);  // < K while the invariant holds
+      if (slot < K) sel[slot] = items[i];
     }
-  }
-  for (int i = threadIdx.x; i < K; i += kThreads) {
-    values[static_cast<long long>(b) * K + i] = key_bits(sel[i]);
-    indices[static_cast<long long>(b) * K + i] = key_index(sel[i]);
-  }
+  __syncthreads();
+  write_sorted_row(sel, K, values + static_cast<long long>(b) * K,
+                   indices + static_cast<long long>(b) * K);
 }
 
 }  // namespace
@@ -507,16 +619,18 @@ cudaError_t launch_topk(const TopkProblem& p, cudaStream_t stream) {
                                static_cast<int>(csmem));
     if (err != cudaSuccess) return err;
     topk_chunk_kernel<true><<<dim3(p.n_chunks, p.B), kThreads, csmem, stream>>>(
-        p.scores, p.row_stride, p.V, p.K, p.chunk, p.n_chunks, p.cand);
+        p.scores, p.row_stride, p.V, p.K, p.chunk, p.n_chunks, p.cand,
+        reinterpret_cast<uint32_t*>(p.values), p.indices);
   } else {
     err = cudaFuncSetAttribute(topk_chunk_kernel<false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(csmem));
     if (err != cudaSuccess) return err;
     topk_chunk_kernel<false><<<dim3(p.n_chunks, p.B), kThreads, csmem, stream>>>(
-        p.scores, p.row_stride, p.V, p.K, p.chunk, p.n_chunks, p.cand);
+        p.scores, p.row_stride, p.V, p.K, p.chunk, p.n_chunks, p.cand,
+        reinterpret_cast<uint32_t*>(p.values), p.indices);
   }
   err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  if (err != cudaSuccess || p.n_chunks == 1) return err;  // one chunk per row: done
   int P = 1;
   while (P < p.K) P <<= 1;
   const size_t smem = (static_cast<size_t>(p.n_chunks) * p.K + P) * sizeof(uint64_t);

@@ -228,7 +228,8 @@ fa_status_t fa_mha_kv_cache_plan(int B, int Sq, int S_cache, int H, int Hkv, int
  *   scores  : device, [B, V] fp32, rows row_stride elements apart (>= V).
  *   B, V, K : 1 <= B <= 65535, V >= 1, 1 <= K <= min(V, 1024).
  *   workspace, workspace_bytes : caller-owned device scratch of at least the
- *             size fa_topk_plan returns for (B, V, K); 8-byte aligned.
+ *             size fa_topk_plan returns for (B, V, K) (may be NULL when that
+ *             size is 0: every row is one chunk); 8-byte aligned.
  *   stream  : cudaStream_t as void*.
  * Asynchronous; argument errors are returned before any CUDA call.
  */

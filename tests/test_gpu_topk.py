@@ -95,6 +95,32 @@ def test_strided_rows():
     _check(x.contiguous(), 77, dev)
 
 
+def test_more_rows_than_one_wave_of_ctas():
+    """More rows than resident CTAs: one chunk per row, several waves, each
+    chunk CTA sorting its own row."""
+    _check(make_scores(700, 3000, 21), 20)
+    _check(make_scores(400, 2500, 22), 200)
+
+
+def test_single_chunk_rows_take_no_workspace():
+    """A plan of one chunk per row needs no workspace: the C ABI accepts NULL."""
+    B, V, K = 256, 8192, 10
+    chunks, ws = fa.topk_plan(B, V, K)
+    assert chunks == 1 and ws == 0
+    x = make_scores(B, V, 23)
+    dev = x.cuda()
+    vals = torch.empty((B, K), dtype=torch.float32, device="cuda")
+    idx = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    lib = fa.load_library()
+    rc = lib.fa_topk(vals.data_ptr(), idx.data_ptr(), dev.data_ptr(), B, V, V, K, None, 0,
+                     torch.cuda.current_stream().cuda_stream)
+    assert rc == fa.FA_OK
+    torch.cuda.synchronize()
+    ref_v, ref_i = topk_oracle.topk(x.numpy(), K)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_i)
+    assert vals.cpu().numpy().tobytes() == ref_v.tobytes()
+
+
 @pytest.mark.parametrize("name", sorted(TOPK_WORKLOADS))
 def test_topk_workload_full_size(name):
     w = TOPK_WORKLOADS[name]

@@ -20,11 +20,23 @@ def test_plan_bounds(lib, B, V, K):
     assert chunks >= 1
     chunk = -(-V // chunks)
     assert chunks * K <= max(4096, K)          # the merge's candidates
-    assert ws == B * chunks * K * 8
+    assert ws == (0 if chunks == 1 else B * chunks * K * 8)  # one chunk: no candidates kept
     # every chunk but the last is a whole number of 2048-element steps
     step_chunk = -(-(-(-V // chunks)) // 2048) * 2048
     assert -(-V // step_chunk) == chunks
     assert chunk <= step_chunk
+
+
+@pytest.mark.parametrize("B", [1, 7, 64, 100, 152, 256, 303, 304, 305, 4096])
+def test_plan_stays_within_one_wave(lib, B):
+    """Chunk CTAs (two resident per SM) fit one wave whenever the rows do."""
+    chunks, _ = fa.topk_plan(B, 1 << 18, 50, num_sms=152)
+    if B <= 304:
+        # at most the requested count (whole 2048-element steps can leave fewer)
+        assert chunks <= min(304 // B, 4096 // 50)
+        assert chunks >= min(304 // B, 4096 // 50) // 2
+    else:
+        assert chunks == 1
 
 
 def test_plan_fills_the_gpu_for_small_batches(lib):
