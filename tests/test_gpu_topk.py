@@ -121,6 +121,31 @@ def test_single_chunk_rows_take_no_workspace():
     assert vals.cpu().numpy().tobytes() == ref_v.tobytes()
 
 
+@pytest.mark.parametrize("B,V,K", [(1, 262144, 50), (1, 262144, 1024), (3, 100000, 1000),
+                                   (2, 300000, 7), (9, 65536, 333)])
+def test_rows_split_over_many_chunks(B, V, K):
+    """Rows spread over several chunk CTAs: each chunk's candidates, merged per
+    row (up to 147 chunks of a row, K up to 1024)."""
+    chunks, ws = fa.topk_plan(B, V, K)
+    assert ws > 0 and chunks > 1
+    _check(make_scores(B, V, 30 + K), K)
+
+
+def test_workspace_reused_across_calls():
+    """Whatever the workspace held before, every call writes the candidates it
+    reads."""
+    B, V, K = 4, 70000, 64
+    _, ws_bytes = fa.topk_plan(B, V, K)
+    ws = torch.full((ws_bytes,), 0xAB, dtype=torch.uint8, device="cuda")
+    for seed in (41, 42, 43):
+        x = make_scores(B, V, seed)
+        vals, idx = fa.topk(x.cuda(), K, workspace=ws)
+        torch.cuda.synchronize()
+        ref_v, ref_i = topk_oracle.topk(x.numpy(), K)
+        np.testing.assert_array_equal(idx.cpu().numpy(), ref_i)
+        assert vals.cpu().numpy().tobytes() == ref_v.tobytes()
+
+
 @pytest.mark.parametrize("name", sorted(TOPK_WORKLOADS))
 def test_topk_workload_full_size(name):
     w = TOPK_WORKLOADS[name]
