@@ -440,7 +440,8 @@ def bench_ours(args, w, world, rank, local, dist):
     achieved = flops / (local_ms / args.steps * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
-                "traffic": profiled_traffic(w.name) if w.dtype == "bf16" else None,
+                "traffic": profiled_traffic(w.name) if w.dtype == "bf16"
+                else profiled_traffic(w.name, "fa_fwd_f32x3_kernel", "fa_fwd_f32x3.cu"),
                 "peak_source": f"{peak_src} ({peak_note})"
                 if peak_src == "measured" else "fallback",
                 "algorithmic_bytes": algorithmic_bytes(w),
