@@ -17,9 +17,10 @@
 //     elements per lane per step, staged by asynchronous 16-byte copies (4-byte
 //     when the rows are not 16-byte aligned) in a shared-memory ring with
 //     seven steps in flight). Before the scan the CTA seeds its threshold
-//     from the first four staged steps: the K-th largest of the per-lane,
-//     per-step maxima (1024 distinct elements), rounded down, is a lower
-//     bound of the chunk's K-th key. A
+//     from the first staged steps (all seven for a long chunk or a large K,
+//     else four): the K-th largest of the per-lane, per-step maxima (1792 or
+//     1024 distinct elements), rounded down, is a lower bound of the chunk's
+//     K-th key. A
 //     warp keeps only keys above the best threshold any warp of the CTA has
 //     published (the value half of the key is compared first), each lane
 //     appending its own rare candidates to a warp-private buffer;
@@ -399,10 +400,13 @@ __device__ void write_sorted_row(uint64_t* keys, int K, uint32_t* values, int* i
 // staging slots (kWarpStep words each), a key buffer of prune_at + kWarpStep
 // keys and a 256-bin histogram, then the CTA's merge area of kWarps * K keys.
 constexpr int kRing = 8;
-constexpr int kSeedSteps = 4;  // scan steps per warp that seed the threshold
-static_assert(kSeedSteps < kRing, "the seed steps are staged by the prologue");
-static_assert(kSeedSteps * kThreads >= kMaxTopK, "at least K groups seed the threshold");
-static_assert(kSeedSteps * kThreads <= kWarps * 2 * kWarpStep, "seed keys fit the key buffers");
+// Scan steps per warp that seed the threshold: all the prologue stages for a
+// long chunk or a large K, fewer for a short chunk, whose few steps cannot
+// amortise waiting for the last staged one.
+constexpr int kSeedStepsLong = kRing - 1;
+constexpr int kSeedStepsShort = 4;
+static_assert(kSeedStepsShort * kThreads >= kMaxTopK, "at least K groups seed the threshold");
+static_assert(kSeedStepsLong * kThreads <= kWarps * 2 * kWarpStep, "seed keys fit the key buffers");
 constexpr int kRingKeys = kWarps * kRing * kWarpStep / 2;  // 64-bit keys the ring holds
 static_assert(kWarps * kMaxTopK <= kRingKeys, "the warps' top K always fit the idle ring");
 static_assert(kWarps >= 2, "the merge area (kWarps * K keys) holds the sort buffer");
@@ -471,19 +475,25 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
   for (int r = 0; r < kRing - 1; ++r) stage(r, r);
 
-  // Seed the CTA's threshold from the first kSeedSteps steps of every warp
+  // Seed the CTA's threshold from the first seed_steps steps of every warp
   // (already staged): per lane and step the largest of its scores, one
   // distinct element per group, as a key whose low half is a distinct id
   // (key 0 marks a group without elements). The value half of the K-th
   // largest of these keys, rounded down by the radix select, is at or below
   // at least K elements of the chunk, so it bounds the chunk's K-th key from
   // below: nothing the top K needs is filtered out. Starting every warp near
-  // the K-th of the 8 * kSeedSteps * kThreads sampled scores instead of from
+  // the K-th of the 8 * seed_steps * kThreads sampled scores instead of from
   // zero leaves a warp with a few dozen candidates per chunk and rarely a
   // prune.
-  cp_async_wait<kRing - 1 - kSeedSteps>();
+  const bool long_seed = steps >= 32 || K > 256;  // uniform over the CTA
+  const int seed_steps = long_seed ? kSeedStepsLong : kSeedStepsShort;
+  if (long_seed)
+    cp_async_wait<kRing - 1 - kSeedStepsLong>();
+  else
+    cp_async_wait<kRing - 1 - kSeedStepsShort>();
 #pragma unroll
-  for (int s = 0; s < kSeedSteps; ++s) {
+  for (int s = 0; s < kSeedStepsLong; ++s) {
+    if (s >= seed_steps) break;
     uint32_t x[kPerThread];
     read_step(ring + s * kWarpStep, x);
     int32_t best = INT_MIN;
@@ -506,7 +516,7 @@ __global__ void __launch_bounds__(kThreads)
   }
   __syncthreads();
   {
-    const Selection seed = block_select_top(wbufs, kSeedSteps * kThreads, K, sc);
+    const Selection seed = block_select_top(wbufs, seed_steps * kThreads, K, sc);
     if (threadIdx.x == 0) s_best = seed.prefix & 0xffffffff00000000ull;
   }
   __syncthreads();  // the key buffers are reused by the scan
