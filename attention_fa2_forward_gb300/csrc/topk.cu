@@ -289,11 +289,11 @@ __device__ __forceinline__ void filter_step(const uint32_t (&x)[kPerThread],
                                             const uint32_t* words, int base, int end, int K,
                                             WarpScan& ws) {
   const int lane = threadIdx.x & 31;
-  // Common path, 4 integer operations per element: the value half of the key
-  // as a signed integer in total order (b ^ ((b >> 31) & 0x7fffffff)) against
-  // the threshold's value half, conservatively (>=); the few elements that
-  // pass get the exact 64-bit test below. Only a chunk's last blocks need the
-  // bounds test.
+  // Common path, 2 to 4 integer operations per element: the value half of the
+  // key as a signed integer in total order (b ^ ((b >> 31) & 0x7fffffff))
+  // against the threshold's value half, conservatively (>=); the few elements
+  // that pass get the exact 64-bit test below. Only a chunk's last blocks
+  // need the bounds test.
   // Any warp's K-th key is a lower bound of the CTA's K-th key: filter
   // against the best one published so far, read during the previous step so
   // that its latency stays off this step's path.
@@ -301,7 +301,14 @@ __device__ __forceinline__ void filter_step(const uint32_t (&x)[kPerThread],
   ws.best_seen = *reinterpret_cast<volatile unsigned long long*>(ws.best);
   const int32_t s_thr = static_cast<int32_t>(static_cast<uint32_t>(ws.thr >> 32) ^ 0x80000000u);
   unsigned mask = 0;
-  if (base + kWarpStep <= end) {
+  if (base + kWarpStep <= end && s_thr >= 0) {
+    // A threshold value >= +0 (the usual case once seeded): raw bits compare
+    // as signed integers directly, negative scores and -NaN being negative
+    // integers below it.
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e)
+      if (static_cast<int32_t>(x[e]) >= s_thr) mask |= 1u << e;
+  } else if (base + kWarpStep <= end) {
 #pragma unroll
     for (int e = 0; e < kPerThread; ++e) {
       const int32_t v = static_cast<int32_t>(x[e]);
