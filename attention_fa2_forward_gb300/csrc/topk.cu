@@ -32,8 +32,11 @@
 //     survivors once (block-wide). A chunk that is the whole row writes
 //     them sorted straight to the output; otherwise they go (padded with key
 //     0, below every real key, when the chunk is shorter) to the workspace;
-//   * merge kernel (rows of several chunks only): one CTA per row selects
-//     the top K of the chunks' candidates the same way.
+//   * rows of 2, 4 or 8 chunks: the row's chunk CTAs form a thread-block
+//     cluster, and its first CTA reads the others' top K from their shared
+//     memory, selects the row's top K and writes it;
+//   * merge kernel (other multi-chunk rows): one CTA per row selects the top
+//     K of the chunks' candidates the same way.
 // Sorting K distinct keys: up to 128 each key's place is its count of
 // larger keys, above that a bitonic sort.
 // Scores are handled as raw 32-bit patterns from load to store: no float
@@ -44,6 +47,7 @@
 #include <cstdint>
 
 #include "fa_internal.h"
+#include "topk_plan.h"
 
 namespace fa {
 namespace {
@@ -64,6 +68,32 @@ __device__ __forceinline__ uint64_t make_key(uint32_t bits, uint32_t index) {
 __device__ __forceinline__ uint32_t key_bits(uint64_t key) {
   const uint32_t t = static_cast<uint32_t>(key >> 32);
   return (t & 0x80000000u) ? (t & 0x7fffffffu) : ~t;
+}
+
+// Thread-block cluster helpers: this CTA's rank in its cluster, a barrier
+// over every thread of the cluster (release / acquire: shared-memory writes
+// before it are visible to the cluster's loads after it), and a load from a
+// peer CTA's shared memory at the same offset as `local` (a shared-window
+// address) in this CTA.
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local, unsigned rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ uint64_t ld_cluster_u64(uint32_t remote) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ int key_index(uint64_t key) {
@@ -429,7 +459,7 @@ template <bool kVec>
 __global__ void __launch_bounds__(kThreads)
     topk_chunk_kernel(const float* __restrict__ scores, long long row_stride, int V, int K,
                       int chunk, int n_chunks, uint64_t* __restrict__ cand,
-                      uint32_t* __restrict__ values, int* __restrict__ indices) {
+                      uint32_t* __restrict__ values, int* __restrict__ indices, int clustered) {
   extern __shared__ uint64_t dyn[];
   __shared__ SelectScratch sc;
   __shared__ int s_count[kWarps];
@@ -586,6 +616,37 @@ __global__ void __launch_bounds__(kThreads)
   if (n_chunks == 1) {  // the chunk is the whole row: its top K is the answer
     write_sorted_row(top, K, values + static_cast<long long>(b) * K,
                      indices + static_cast<long long>(b) * K);
+  } else if (clustered) {
+    // The row's chunk CTAs form one cluster (rank = chunk): rank 0 reads the
+    // others' top K from their shared memory, selects the row's top K and
+    // writes it. The keys of a row are distinct and every chunk gave
+    // min(K, its length) real keys, so the K largest are real; padding keys
+    // (0) sort below them.
+    cluster_sync();  // every chunk's top K is in its shared memory
+    if (cluster_rank() == 0) {
+      const int n = n_chunks * K;  // <= kRingKeys
+      uint64_t* gathered = reinterpret_cast<uint64_t*>(rings);
+      const uint32_t top_s = static_cast<uint32_t>(__cvta_generic_to_shared(top));
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int r = i / K, e = i - r * K;
+        gathered[i] = r == 0 ? top[e] : ld_cluster_u64(cluster_map(top_s + 8u * e, r));
+      }
+      __syncthreads();
+      const Selection sel = block_select_top(gathered, n, K, sc);
+      if (threadIdx.x == 0) sc.count = 0;
+      __syncthreads();
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint64_t v = gathered[i];
+        if ((v & sel.mask) >= sel.prefix) {
+          const int slot = atomicAdd(&sc.count, 1);  // < K while the invariant holds
+          if (slot < K) top[slot] = v;
+        }
+      }
+      __syncthreads();
+      write_sorted_row(top, K, values + static_cast<long long>(b) * K,
+                       indices + static_cast<long long>(b) * K);
+    }
+    cluster_sync();  // no CTA leaves while rank 0 may still read its shared memory
   } else {
     uint64_t* dst = cand + (static_cast<long long>(b) * n_chunks + c) * K;
     for (int i = threadIdx.x; i < K; i += kThreads) dst[i] = top[i];
@@ -630,24 +691,37 @@ cudaError_t launch_topk(const TopkProblem& p, cudaStream_t stream) {
                    p.V % 4 == 0;
   if (p.chunk % (kWarps * kWarpStep) != 0) return cudaErrorInvalidValue;
   const size_t csmem = chunk_smem_bytes(p.K);
-  cudaError_t err;
-  if (vec) {
-    err = cudaFuncSetAttribute(topk_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(csmem));
-    if (err != cudaSuccess) return err;
-    topk_chunk_kernel<true><<<dim3(p.n_chunks, p.B), kThreads, csmem, stream>>>(
-        p.scores, p.row_stride, p.V, p.K, p.chunk, p.n_chunks, p.cand,
-        reinterpret_cast<uint32_t*>(p.values), p.indices);
-  } else {
-    err = cudaFuncSetAttribute(topk_chunk_kernel<false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(csmem));
-    if (err != cudaSuccess) return err;
-    topk_chunk_kernel<false><<<dim3(p.n_chunks, p.B), kThreads, csmem, stream>>>(
-        p.scores, p.row_stride, p.V, p.K, p.chunk, p.n_chunks, p.cand,
-        reinterpret_cast<uint32_t*>(p.values), p.indices);
-  }
+  const bool clustered = topk_clustered(p.n_chunks) && p.n_chunks > 1;
+  static_assert(kTopkMaxCluster * kMaxTopK <= kRingKeys, "a cluster's candidates fit the ring");
+  auto launch = [&](auto kernel) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(csmem));
+    if (e != cudaSuccess) return e;
+    uint32_t* vals = reinterpret_cast<uint32_t*>(p.values);
+    if (!clustered) {
+      kernel<<<dim3(p.n_chunks, p.B), kThreads, csmem, stream>>>(
+          p.scores, p.row_stride, p.V, p.K, p.chunk, p.n_chunks, p.cand, vals, p.indices, 0);
+      return cudaSuccess;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_chunks, p.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = csmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.n_chunks);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p.scores, p.row_stride, p.V, p.K, p.chunk,
+                              p.n_chunks, p.cand, vals, p.indices, 1);
+  };
+  cudaError_t err = vec ? launch(topk_chunk_kernel<true>) : launch(topk_chunk_kernel<false>);
+  if (err != cudaSuccess) return err;
   err = cudaGetLastError();
-  if (err != cudaSuccess || p.n_chunks == 1) return err;  // one chunk per row: done
+  if (err != cudaSuccess || p.n_chunks == 1 || clustered) return err;  // rows already finished
   int P = 1;
   while (P < p.K) P <<= 1;
   const size_t smem = (static_cast<size_t>(p.n_chunks) * p.K + P) * sizeof(uint64_t);

@@ -822,8 +822,9 @@ def bench_topk_ours(args, w, world, rank, local, dist):
                              "hides host launch latency (e2e includes it)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        # one chunk per row: the chunk kernel finishes each row; otherwise a merge follows
-        "clocks": clocks.summary(), "gpu_launches": args.steps * (1 if chunks == 1 else 2),
+        # rows of 1, 2, 4 or 8 chunks are finished by the chunk kernel (no workspace);
+        # other plans add a merge kernel
+        "clocks": clocks.summary(), "gpu_launches": args.steps * (1 if ws_bytes == 0 else 2),
     }
 
 

@@ -125,10 +125,22 @@ def test_single_chunk_rows_take_no_workspace():
                                    (2, 300000, 7), (9, 65536, 333)])
 def test_rows_split_over_many_chunks(B, V, K):
     """Rows spread over several chunk CTAs: each chunk's candidates, merged per
-    row (up to 147 chunks of a row, K up to 1024)."""
+    row by the merge kernel or inside a cluster (up to 147 chunks of a row, K
+    up to 1024)."""
     chunks, ws = fa.topk_plan(B, V, K)
-    assert ws > 0 and chunks > 1
+    assert chunks > 1
+    assert (ws == 0) == (chunks in (2, 4, 8))  # clusters of 2, 4, 8 merge in shared memory
     _check(make_scores(B, V, 30 + K), K)
+
+
+@pytest.mark.parametrize("B,V,K,chunks", [(152, 8192, 10, 2), (64, 131072, 300, 4),
+                                          (38, 65536, 64, 8), (38, 65536, 1000, 4)])
+def test_rows_merged_inside_a_cluster(B, V, K, chunks):
+    """Rows of 2, 4 or 8 chunks: the chunk CTAs of a row form one cluster whose
+    first CTA merges the others' candidates from their shared memory."""
+    got_chunks, ws = fa.topk_plan(B, V, K)
+    assert got_chunks == chunks and ws == 0
+    _check(make_scores(B, V, 60 + chunks + K), K)
 
 
 def test_workspace_reused_across_calls():
