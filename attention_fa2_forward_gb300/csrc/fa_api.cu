@@ -372,9 +372,9 @@ TopkPlan make_topk_plan(int B, int V, int K, int num_sms) {
   TopkPlan t;
   t.chunk = static_cast<int>(chunk);
   t.n_chunks = static_cast<int>((V + chunk - 1) / chunk);
-  // A row of one chunk is finished by its chunk CTA, a row of 2, 4 or 8 by its
-  // cluster's first CTA: no candidates to keep in either case.
-  t.workspace_bytes = fa::topk_clustered(t.n_chunks)
+  // A row of one chunk is finished by its chunk CTA, a row of 2, 4 or 8 (K up
+  // to 128) by its cluster's first CTA: no candidates to keep in either case.
+  t.workspace_bytes = fa::topk_clustered(t.n_chunks, K)
                           ? 0ull
                           : static_cast<unsigned long long>(B) * t.n_chunks * K * 8ull;
   return t;

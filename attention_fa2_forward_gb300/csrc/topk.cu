@@ -32,9 +32,9 @@
 //     survivors once (block-wide). A chunk that is the whole row writes
 //     them sorted straight to the output; otherwise they go (padded with key
 //     0, below every real key, when the chunk is shorter) to the workspace;
-//   * rows of 2, 4 or 8 chunks: the row's chunk CTAs form a thread-block
-//     cluster, and its first CTA reads the others' top K from their shared
-//     memory, selects the row's top K and writes it;
+//   * rows of 2, 4 or 8 chunks with K <= 128: the row's chunk CTAs form a
+//     thread-block cluster, and its first CTA reads the others' top K from
+//     their shared memory, selects the row's top K and writes it;
 //   * merge kernel (other multi-chunk rows): one CTA per row selects the top
 //     K of the chunks' candidates the same way.
 // Sorting K distinct keys: up to 128 each key's place is its count of
@@ -691,7 +691,12 @@ cudaError_t launch_topk(const TopkProblem& p, cudaStream_t stream) {
                    p.V % 4 == 0;
   if (p.chunk % (kWarps * kWarpStep) != 0) return cudaErrorInvalidValue;
   const size_t csmem = chunk_smem_bytes(p.K);
-  const bool clustered = topk_clustered(p.n_chunks) && p.n_chunks > 1;
+  const bool clustered = topk_clustered(p.n_chunks, p.K) && p.n_chunks > 1;
+  static_assert(2 * (kWarps * kRing * kWarpStep * sizeof(uint32_t) +
+                     kWarps * (256 + kWarpStep) * sizeof(uint64_t) +
+                     kWarps * 256 * sizeof(unsigned) + kWarps * kTopkClusterMaxK * sizeof(uint64_t) +
+                     2048) <= 228 * 1024,
+                "two chunk CTAs share an SM up to the largest clustered K");
   static_assert(kTopkMaxCluster * kMaxTopK <= kRingKeys, "a cluster's candidates fit the ring");
   auto launch = [&](auto kernel) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

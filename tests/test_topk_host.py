@@ -20,8 +20,9 @@ def test_plan_bounds(lib, B, V, K):
     assert chunks >= 1
     chunk = -(-V // chunks)
     assert chunks * K <= max(4096, K)          # the merge's candidates
-    # one chunk, or a cluster of 2, 4 or 8: no candidates kept in the workspace
-    assert ws == (0 if chunks in (1, 2, 4, 8) else B * chunks * K * 8)
+    # one chunk, or a cluster of 2, 4 or 8 (K <= 128): no candidates kept
+    clustered = chunks == 1 or (chunks in (2, 4, 8) and K <= 128)
+    assert ws == (0 if clustered else B * chunks * K * 8)
     # every chunk but the last is a whole number of 2048-element steps
     step_chunk = -(-(-(-V // chunks)) // 2048) * 2048
     assert -(-V // step_chunk) == chunks
