@@ -145,6 +145,36 @@ def test_rows_merged_inside_a_cluster(B, V, K, chunks):
     _check(make_scores(B, V, 60 + chunks + K), K)
 
 
+def test_special_values_inside_a_cluster():
+    """NaNs of both signs, infinities, signed zeros and all-negative rows on the
+    cluster path (8 chunks per row, K <= 128): bit-exact against the oracle."""
+    B, V, K = 38, 65536, 64
+    assert fa.topk_plan(B, V, K)[0] == 8
+    g = torch.Generator().manual_seed(70)
+    x = torch.randn((B, V), generator=g)
+    x[0, ::97] = float("nan")
+    x[1, 5:300] = NEG_NAN
+    x[2, 1000:1100] = float("inf")
+    x[3, :] = -x[3, :].abs() - 1.0                     # every score negative
+    x[4, :] = float("-inf")                            # every score -inf
+    x[5, ::2] = 0.0
+    x[5, 1::2] = -0.0
+    x[6, 60000:] = float("inf")                        # the top K all in the last chunk
+    _check(x, K)
+
+
+def test_negative_thresholds_and_unaligned_rows():
+    """Rows whose K-th score is negative (the total-order test on the scan's
+    common path) and rows that are not 16-byte aligned (4-byte copies)."""
+    g = torch.Generator().manual_seed(71)
+    x = -torch.rand((6, 20001), generator=g) - 0.5
+    _check(x, 40)
+    wide = torch.randn((5, 30003), generator=g)
+    dev = wide.cuda()[:, 1:30001]
+    assert dev.stride(0) == 30003 and dev.data_ptr() % 16 != 0
+    _check(wide[:, 1:30001].contiguous(), 33, dev)
+
+
 def test_workspace_reused_across_calls():
     """Whatever the workspace held before, every call writes the candidates it
     reads."""
