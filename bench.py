@@ -211,6 +211,19 @@ def pipelined_e2e_ms(n_steps, copy_in, compute, copy_out, stream):
     return e0.elapsed_time(e1) / n_steps
 
 
+def prefill_traffic(w):
+    """Profiled DRAM bytes per launch of the kernel that serves workload w:
+    the bf16 tensor-core kernel up to D = 128, the one-Q-tile kernel above, the
+    fp32 tensor-core kernel for fp32 D 64/128 (none for the CUDA-core path)."""
+    if w.dtype == "bf16":
+        if w.D > 128:
+            return profiled_traffic(w.name, KV_KERNEL_NAME, "fa_decode_tc.cu")
+        return profiled_traffic(w.name)
+    if w.D in (64, 128):
+        return profiled_traffic(w.name, "fa_fwd_f32x3_kernel", "fa_fwd_f32x3.cu")
+    return None
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     """Samples SM clock and clock-event reasons through NVML (ctypes) while the
@@ -484,8 +497,7 @@ def bench_ours(args, w, world, rank, local, dist):
     achieved = flops / (local_ms / args.steps * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
-                "traffic": profiled_traffic(w.name) if w.dtype == "bf16"
-                else profiled_traffic(w.name, "fa_fwd_f32x3_kernel", "fa_fwd_f32x3.cu"),
+                "traffic": prefill_traffic(w),
                 "peak_source": f"{peak_src} ({peak_note})"
                 if peak_src == "measured" else "fallback",
                 "algorithmic_bytes": algorithmic_bytes(w),
