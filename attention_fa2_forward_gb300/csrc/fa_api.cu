@@ -320,12 +320,24 @@ KvPlan make_kv_plan(int B, int Sq, int S_cache, int H, int Hkv, int D, int causa
   long long splits = num_splits;
   if (splits == 0) {
     // Auto. Units (batch x KV head x position tile) that fill half the SMs
-    // stream best unsplit (one CTA each, no combine). Fewer units are cut so
-    // that about 1.5 CTAs per SM exist: enough for the HBM stream, and when
-    // the lengths are ragged (unknown here: they live on the device) the
-    // splits of short sequences finish early and free their SMs for others.
+    // stream best unsplit (one CTA each, no combine). Fewer units are cut:
+    //  * very few (at most one per 8 SMs: a few long sequences) into about
+    //    0.75 x SMs CTAs -- one CTA per SM streams about 54 GB/s, and past
+    //    ~128 concurrent streams the HBM gives each less than the extra
+    //    streams add (14 splits of one 131072-key sequence: 89 % of the HBM
+    //    peak, 19: 82 %, 22, a second wave of 24 CTAs: 65 %);
+    //  * more, whose lengths may be ragged (unknown here: they live on the
+    //    device), into about two CTAs per SM, so that the splits of short
+    //    sequences finish early and free their SMs for the long ones.
     const long long units = static_cast<long long>(B) * Hkv * k.n_ptiles;
-    splits = 2 * units >= num_sms ? 1 : (3ll * num_sms + 2 * units - 1) / (2 * units);
+    if (2 * units >= num_sms) {
+      splits = 1;
+    } else if (8 * units <= num_sms) {
+      splits = (3ll * num_sms) / (4 * units);
+      if (splits < 1) splits = 1;
+    } else {
+      splits = (2ll * num_sms + units / 2) / units;  // rounded
+    }
   }
   if (splits > kMaxSplits) splits = kMaxSplits;
   if (splits > max_tiles) splits = max_tiles;

@@ -30,6 +30,13 @@ def _expected_splits(req, tiles):
     return -(-tiles // per)
 
 
+def test_auto_split_requests_of_the_decode_workloads():
+    # one 131072-key sequence x 8 KV heads: 14 splits (112 CTAs); a ragged
+    # batch of 8 x 8 KV heads: 5 (320 CTAs, short splits finish early)
+    assert _plan(1, 1, 131072, 32, 8, 128)[0] == 14
+    assert _plan(8, 4, 32768, 32, 8, 128)[0] == 5
+
+
 def test_enough_units_take_one_split():
     # 16 batches x 8 KV heads = 128 units: one split, no workspace; 76 units
     # (half of 152 SMs) still one.
@@ -38,12 +45,22 @@ def test_enough_units_take_one_split():
     assert _plan(37, 1, 8192, 8, 2, 128)[0] > 1
 
 
+def _auto_request(units, sms=152):
+    """The automatic split request: a few long units into ~0.75 x SMs CTAs,
+    more units into ~2 CTAs per SM (rounded)."""
+    if 2 * units >= sms:
+        return 1
+    if 8 * units <= sms:
+        return max(1, 3 * sms // (4 * units))
+    return (2 * sms + units // 2) // units
+
+
 @pytest.mark.parametrize("B,Hkv,S", [(1, 8, 131072), (2, 8, 32768), (1, 1, 65536), (4, 4, 8192),
                                      (8, 8, 32768)])
 def test_few_units_are_split_to_fill_the_gpu(B, Hkv, S):
     splits, ws = _plan(B, 1, S, 8 * Hkv, Hkv, 128)
     units = B * Hkv
-    assert splits == _expected_splits(-(-3 * 152 // (2 * units)), _tiles(S))
+    assert splits == _expected_splits(_auto_request(units), _tiles(S))
     rows = B * 8 * Hkv
     expect = ((splits * rows * 128 * 4 + 255) // 256 * 256) + ((splits * rows * 4 + 255) // 256 * 256)
     assert ws == expect
@@ -70,8 +87,8 @@ def test_position_tiles_count_as_units():
     # Sq = 64 with 4 heads per KV head: 2 position tiles of 32 positions.
     s1, _ = _plan(1, 64, 16384, 8, 2, 128)
     s2, _ = _plan(1, 32, 16384, 8, 2, 128)
-    assert s1 == _expected_splits(-(-3 * 152 // 8), 128)
-    assert s2 == _expected_splits(-(-3 * 152 // 4), 128)
+    assert s1 == _expected_splits(_auto_request(4), 128)   # 2 KV heads x 2 position tiles
+    assert s2 == _expected_splits(_auto_request(2), 128)
 
 
 P = 0x10000  # a non-null, 16-byte aligned fake address: never dereferenced
