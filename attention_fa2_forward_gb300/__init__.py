@@ -23,7 +23,7 @@ import threading
 
 import torch
 
-from .build import LIB_PATH, build  # noqa: F401  (re-exported)
+from .build import DEBUG_LIB_PATH, LIB_PATH, build  # noqa: F401  (re-exported)
 
 MASK_NONE = 0
 MASK_CAUSAL = 1
@@ -35,16 +35,20 @@ FA_ERR_INVALID_ARG = 1
 FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
+FA_ERR_BOUNDS = 5
 
 # Every symbol the header declares (checked by the tests).
 EXPORTS = ("fa_mha_no_cache", "fa_mha_no_cache_strided", "fa_mha_no_cache_noalloc",
+           "fa_mha_no_cache_host", "fa_mha_no_cache_host_workspace",
            "fa_mha_no_cache_f32_tc", "fa_mha_no_cache_f32_tc_workspace",
            "fa_mha_kv_cache", "fa_mha_kv_cache_plan", "fa_topk", "fa_topk_plan",
-           "fa_device_status",
+           "fa_stream_status", "fa_device_status",
            "fa_set_wait_timeout_ns", "fa_set_stall_probe", "fa_status_string",
-           "fa_last_error_message", "fa_version", "fa_shutdown")
+           "fa_last_error_message", "fa_version", "fa_trace_set_buffer",
+           "fa_trace_bytes_per_cta", "fa_trace_ctas", "fa_debug_set_lse_limit", "fa_shutdown")
 
 _lib = None
+_debug_lib = None
 _lock = threading.Lock()
 
 
@@ -60,53 +64,88 @@ def load_library(path: str | None = None):
     with _lock:
         if _lib is not None and path is None:
             return _lib
-        p = path or LIB_PATH
-        if not os.path.exists(p):
-            raise RuntimeError(
-                f"CUDA library {p} is not built; call attention_fa2_forward_gb300.build() "
-                "(nvcc, sm_103a) first")
-        lib = ctypes.CDLL(p)
-        vp, i = ctypes.c_void_p, ctypes.c_int
-        lib.fa_mha_no_cache.restype = i
-        lib.fa_mha_no_cache.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float,
-                                        i, i, i, vp]
-        lp = ctypes.POINTER(ctypes.c_longlong)
-        lib.fa_mha_no_cache_strided.restype = i
-        lib.fa_mha_no_cache_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, lp, lp, lp, lp,
-                                                ctypes.c_float, i, i, i, vp]
-        ull = ctypes.c_ulonglong
-        lib.fa_mha_kv_cache.restype = i
-        lib.fa_mha_kv_cache.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float,
-                                        i, i, i, vp, ull, i, vp]
-        lib.fa_mha_kv_cache_plan.restype = i
-        lib.fa_mha_kv_cache_plan.argtypes = [i, i, i, i, i, i, i, i, i, i,
-                                             ctypes.POINTER(i), ctypes.POINTER(ull)]
-        lib.fa_mha_no_cache_f32_tc.restype = i
-        lib.fa_mha_no_cache_f32_tc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float,
-                                               i, i, vp, ull, vp]
-        lib.fa_mha_no_cache_f32_tc_workspace.restype = ull
-        lib.fa_mha_no_cache_f32_tc_workspace.argtypes = [i, i, i, i]
-        lib.fa_topk.restype = i
-        lib.fa_topk.argtypes = [vp, vp, vp, i, i, ctypes.c_longlong, i, vp, ull, vp]
-        lib.fa_topk_plan.restype = i
-        lib.fa_topk_plan.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(ull)]
-        lib.fa_device_status.restype = i
-        lib.fa_device_status.argtypes = [i, i]
-        lib.fa_set_wait_timeout_ns.restype = ctypes.c_ulonglong
-        lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
-        lib.fa_set_stall_probe.restype = i
-        lib.fa_set_stall_probe.argtypes = [i]
-        lib.fa_status_string.restype = ctypes.c_char_p
-        lib.fa_status_string.argtypes = [i]
-        lib.fa_last_error_message.restype = ctypes.c_char_p
-        lib.fa_last_error_message.argtypes = []
-        lib.fa_version.restype = i
-        lib.fa_version.argtypes = []
-        lib.fa_shutdown.restype = None
-        lib.fa_shutdown.argtypes = []
+        lib = _open(path or LIB_PATH)
         if path is None:
             _lib = lib
         return lib
+
+
+def load_debug_library():
+    """Open the debug build libfa_mha_debug.so (event trace, bounds guards),
+    building it first if needed."""
+    global _debug_lib
+    build(variant="debug")
+    with _lock:
+        if _debug_lib is None:
+            _debug_lib = _open(DEBUG_LIB_PATH)
+        return _debug_lib
+
+
+def _open(p: str):
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"CUDA library {p} is not built; call attention_fa2_forward_gb300.build() "
+            "(nvcc, sm_103a) first")
+    lib = ctypes.CDLL(p)
+    _declare(lib)
+    return lib
+
+
+def _declare(lib):
+    """Declare the C signatures of include/fa_mha.h on a loaded library."""
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.fa_mha_no_cache.restype = i
+    lib.fa_mha_no_cache.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float,
+                                    i, i, i, vp]
+    lp = ctypes.POINTER(ctypes.c_longlong)
+    lib.fa_mha_no_cache_strided.restype = i
+    lib.fa_mha_no_cache_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, lp, lp, lp, lp,
+                                            ctypes.c_float, i, i, i, vp]
+    ull = ctypes.c_ulonglong
+    lib.fa_mha_kv_cache.restype = i
+    lib.fa_mha_kv_cache.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.c_float,
+                                    i, i, i, vp, ull, i, vp]
+    lib.fa_mha_kv_cache_plan.restype = i
+    lib.fa_mha_kv_cache_plan.argtypes = [i, i, i, i, i, i, i, i, i, i,
+                                         ctypes.POINTER(i), ctypes.POINTER(ull)]
+    lib.fa_mha_no_cache_f32_tc.restype = i
+    lib.fa_mha_no_cache_f32_tc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float,
+                                           i, i, vp, ull, vp]
+    lib.fa_mha_no_cache_host.restype = i
+    lib.fa_mha_no_cache_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float,
+                                         i, i, i, vp, ull, vp]
+    lib.fa_mha_no_cache_host_workspace.restype = ull
+    lib.fa_mha_no_cache_host_workspace.argtypes = [i, i, i, i, i, i]
+    lib.fa_mha_no_cache_f32_tc_workspace.restype = ull
+    lib.fa_mha_no_cache_f32_tc_workspace.argtypes = [i, i, i, i]
+    lib.fa_topk.restype = i
+    lib.fa_topk.argtypes = [vp, vp, vp, i, i, ctypes.c_longlong, i, vp, ull, vp]
+    lib.fa_topk_plan.restype = i
+    lib.fa_topk_plan.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(ull)]
+    lib.fa_device_status.restype = i
+    lib.fa_device_status.argtypes = [i, i]
+    lib.fa_stream_status.restype = i
+    lib.fa_stream_status.argtypes = [vp, i]
+    lib.fa_trace_set_buffer.restype = i
+    lib.fa_trace_set_buffer.argtypes = [vp, ull]
+    lib.fa_trace_bytes_per_cta.restype = ull
+    lib.fa_trace_bytes_per_cta.argtypes = []
+    lib.fa_trace_ctas.restype = ctypes.c_longlong
+    lib.fa_trace_ctas.argtypes = [i, i, i, i]
+    lib.fa_debug_set_lse_limit.restype = i
+    lib.fa_debug_set_lse_limit.argtypes = [ctypes.c_longlong]
+    lib.fa_set_wait_timeout_ns.restype = ctypes.c_ulonglong
+    lib.fa_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+    lib.fa_set_stall_probe.restype = i
+    lib.fa_set_stall_probe.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_last_error_message.restype = ctypes.c_char_p
+    lib.fa_last_error_message.argtypes = []
+    lib.fa_version.restype = i
+    lib.fa_version.argtypes = []
+    lib.fa_shutdown.restype = None
+    lib.fa_shutdown.argtypes = []
 
 
 def status_string(status: int) -> str:
@@ -212,6 +251,52 @@ def mha_no_cache(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float
                 dtype, st.cuda_stream)
     _check(rc)
     return (out, lse) if return_lse else out
+
+
+def host_workspace_bytes(B: int, S: int, H: int, Hkv: int, D: int, dtype: torch.dtype) -> int:
+    """Device bytes :func:`mha_no_cache_host` needs for these sizes."""
+    return int(load_library().fa_mha_no_cache_host_workspace(
+        int(B), int(S), int(H), int(Hkv), int(D), _dtype_code(dtype)))
+
+
+def mha_no_cache_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                      workspace: torch.Tensor, scale: float | None = None, mask="causal",
+                      window: int = -1, *, lse: torch.Tensor | None = None,
+                      stream: torch.cuda.Stream | None = None):
+    """The forward on HOST tensors (q, k, v, out, lse: contiguous CPU tensors,
+    pinned for asynchronous copies): one C call enqueues the copies in, the
+    kernel and the copies out on ``stream`` (default: the current stream of
+    the workspace's device). ``workspace`` is a CUDA tensor of at least
+    :func:`host_workspace_bytes` bytes. Returns after enqueueing; synchronise
+    the stream before reading ``out``."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D (BSHD)")
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != S or k.shape[3] != D:
+        raise ValueError("k/v shape does not match q (expected [B, S, Hkv, D])")
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be a contiguous host tensor of q's dtype")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if lse is not None and (lse.is_cuda or lse.shape != (B, H, S) or lse.dtype != torch.float32
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [B, H, S] host tensor")
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    lib = load_library()
+    with torch.cuda.device(workspace.device):
+        st = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+        rc = lib.fa_mha_no_cache_host(
+            out.data_ptr(), lse.data_ptr() if lse is not None else None, q.data_ptr(),
+            k.data_ptr(), v.data_ptr(), B, S, H, Hkv, D, float(scale), _mask_code(mask),
+            int(window), _dtype_code(q.dtype), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), st.cuda_stream)
+    _check(rc)
+    return out
 
 
 def kv_cache_plan(B: int, Sq: int, S_cache: int, H: int, Hkv: int, D: int, mask="causal",
@@ -356,10 +441,19 @@ def topk(scores: torch.Tensor, k: int, *, values: torch.Tensor | None = None,
 
 
 def device_status(device: int | None = None, clear: bool = True) -> int:
-    """Synchronise the device and return its sticky status (FA_OK or FA_ERR_TIMEOUT)."""
+    """Synchronise the device and return the sticky status of all its streams
+    (FA_OK, FA_ERR_TIMEOUT, or FA_ERR_BOUNDS from the debug build)."""
     if device is None:
         device = torch.cuda.current_device()
     return int(load_library().fa_device_status(int(device), int(bool(clear))))
+
+
+def stream_status(stream: torch.cuda.Stream | None = None, clear: bool = True, lib=None) -> int:
+    """Synchronise one stream (default: the current one) and return the sticky
+    status of the work enqueued on it (FA_OK, FA_ERR_TIMEOUT, FA_ERR_BOUNDS)."""
+    st = stream if stream is not None else torch.cuda.current_stream()
+    with torch.cuda.device(st.device):
+        return int((lib or load_library()).fa_stream_status(st.cuda_stream, int(bool(clear))))
 
 
 def set_wait_timeout_ns(ns: int) -> int:

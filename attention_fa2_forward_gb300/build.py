@@ -5,6 +5,11 @@ under _build/, then linked into one shared library exporting the C ABI of
 include/fa_mha.h. The CUDA runtime is linked statically; the driver's
 tensor-map encoder is resolved at run time, so loading the library needs no
 GPU and no libcuda.
+
+The debug variant (``build(variant="debug")``, ``_build/debug/libfa_mha_debug.so``)
+compiles the same sources with FA_TRACE=1: the prefill kernel records an
+event trace into a caller buffer and checks its run-time indexes with bounds
+guards that set a status bit instead of trapping.
 """
 from __future__ import annotations
 
@@ -19,6 +24,10 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libfa_mha.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+DEBUG_DIR = os.path.join(BUILD_DIR, "debug")
+DEBUG_LIB_PATH = os.path.join(DEBUG_DIR, "libfa_mha_debug.so")
+VARIANTS = {"default": (BUILD_DIR, LIB_PATH, []),
+            "debug": (DEBUG_DIR, DEBUG_LIB_PATH, ["-DFA_TRACE=1"])}
 HEADER = os.path.join(ROOT, "include", "fa_mha.h")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -43,25 +52,29 @@ def _inputs() -> list[str]:
     return deps
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(variant: str = "default") -> bool:
+    lib = VARIANTS[variant][1]
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Build libfa_mha.so if any source is newer than it; return its path."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          variant: str = "default") -> str:
+    """Build the library variant ("default": libfa_mha.so, "debug":
+    libfa_mha_debug.so) if any source is newer than it; return its path."""
+    build_dir, lib_path, defines = VARIANTS[variant]
+    if not force and up_to_date(variant):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
-        cmd = [nvcc, *ARCH_FLAGS, *COMMON_FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH_FLAGS, *COMMON_FLAGS, *defines, "-c", src, "-o", obj]
         if ptxas_info:
             cmd.insert(1, "-Xptxas=-v")
         if verbose:
@@ -77,11 +90,12 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             failed.append(src)
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     subprocess.run([nvcc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                variant="debug" if "--debug" in sys.argv else "default"))

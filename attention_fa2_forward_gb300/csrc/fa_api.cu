@@ -1,7 +1,8 @@
 // fa_api.cu -- the C ABI declared in include/fa_mha.h: argument validation,
-// per-device state (status word), TMA tensor-map encoding and dispatch to the
-// bf16 tensor-core kernel or the fp32 CUDA-core kernel, and the KV-cache
-// entry points (work plan: tile geometry, key-range splits, workspace).
+// per-device state (per-stream status words, cached tensor maps and kernel
+// attributes), TMA tensor-map encoding and dispatch to the bf16 tensor-core
+// kernel or the fp32 kernels, and the KV-cache and top-K entry points (work
+// plans: tile geometry, key-range splits, chunks, workspace).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -12,9 +13,11 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "fa_mha.h"
 #include "fa_internal.h"
+#include "fa_trace.cuh"
 #include "topk_plan.h"
 
 namespace {
@@ -24,10 +27,25 @@ constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;
 
 std::mutex g_mutex;
-unsigned* g_status[kMaxDevices] = {};
+
+// Status words, one per stream, per device: a device array of kStatusSlots
+// words allocated on the device's first launch. Streams get slots in the
+// order they are first used; once the array is full, further streams share
+// its last word.
+constexpr int kStatusSlots = 1024;
+struct StatusPool {
+  unsigned* words = nullptr;  // device, kStatusSlots words
+  std::unordered_map<const void*, int> slot_of;
+};
+StatusPool g_pool[kMaxDevices];
 std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<int> g_stall_probe{0};
 thread_local char t_message[512] = "";
+// Debug build only: event trace buffer of the prefill kernel and the LSE
+// bound its guard enforces (0: the LSE tensor's size).
+std::atomic<void*> g_trace_buf{nullptr};
+std::atomic<unsigned long long> g_trace_bytes{0};
+std::atomic<long long> g_lse_limit{0};
 
 fa_status_t fail(fa_status_t st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 fa_status_t fail(fa_status_t st, const char* fmt, ...) {
@@ -73,24 +91,87 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Status word of the current device, created on first use.
-fa_status_t device_status_word(int dev, unsigned** out) {
+// Status word of `stream` on device `dev` (the current device), created on
+// first use.
+fa_status_t stream_status_word(int dev, const void* stream, unsigned** out) {
   if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_status[dev] == nullptr) {
+  StatusPool& pool = g_pool[dev];
+  if (pool.words == nullptr) {
     unsigned* p = nullptr;
-    cudaError_t err = cudaMalloc(&p, sizeof(unsigned));
-    if (err != cudaSuccess) return cuda_fail(err, "cudaMalloc(status word)");
-    err = cudaMemset(p, 0, sizeof(unsigned));
+    cudaError_t err = cudaMalloc(&p, kStatusSlots * sizeof(unsigned));
+    if (err != cudaSuccess) return cuda_fail(err, "cudaMalloc(status words)");
+    err = cudaMemset(p, 0, kStatusSlots * sizeof(unsigned));
+    if (err == cudaSuccess) err = cudaDeviceSynchronize();
     if (err != cudaSuccess) {
       cudaFree(p);
-      return cuda_fail(err, "cudaMemset(status word)");
+      return cuda_fail(err, "cudaMemset(status words)");
     }
-    g_status[dev] = p;
+    pool.words = p;
   }
-  *out = g_status[dev];
+  auto it = pool.slot_of.find(stream);
+  int slot;
+  if (it != pool.slot_of.end()) {
+    slot = it->second;
+  } else {
+    slot = static_cast<int>(pool.slot_of.size());
+    if (slot >= kStatusSlots - 1) {
+      slot = kStatusSlots - 1;  // shared by every stream past the first 1023
+    } else {
+      pool.slot_of.emplace(stream, slot);
+    }
+  }
+  *out = pool.words + slot;
   return FA_OK;
 }
+
+// Status code for the bits of a status word.
+fa_status_t status_from_bits(unsigned bits, const char* where) {
+  if (bits & fa::kStatusWaitTimeout)
+    return fail(FA_ERR_TIMEOUT, "a kernel on %s gave up on a bounded wait", where);
+  if (bits & fa::kStatusBoundsGuard)
+    return fail(FA_ERR_BOUNDS, "a bounds guard of the debug build skipped an access on %s", where);
+  return FA_OK;
+}
+
+// Whether device `dev` is sm_103 (asked once per device).
+fa_status_t check_arch(int dev) {
+  static std::atomic<int> known[kMaxDevices];  // 0 unknown, 1 sm_103, 2 other
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
+  int k = known[dev].load(std::memory_order_acquire);
+  if (k == 1) return FA_OK;
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) {
+    known[dev].store(2, std::memory_order_release);
+    return fail(FA_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+  }
+  known[dev].store(1, std::memory_order_release);
+  return FA_OK;
+}
+
+// Cache of encoded tensor maps, keyed on every encoding argument.
+struct MapKey {
+  const void* base;
+  long long dims[4];
+  long long strides[3];
+  int box_heads, box_rows;
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(*this)) == 0; }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    // FNV-1a over the key's bytes (the key has no padding: checked below).
+    const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < sizeof(k); ++i) h = (h ^ b[i]) * 1099511628211ull;
+    return static_cast<size_t>(h);
+  }
+};
+static_assert(sizeof(MapKey) == 8 + 4 * 8 + 3 * 8 + 2 * 4, "MapKey must have no padding");
+constexpr size_t kMapCacheMax = 4096;  // entries; the cache is emptied when it would grow past
+std::mutex g_map_mutex;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
 
 }  // namespace
 
@@ -98,11 +179,45 @@ namespace fa {
 
 void record_error_message(const char* msg) { snprintf(t_message, sizeof(t_message), "%s", msg); }
 
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+cudaError_t ensure_smem_attr(unsigned long long* done, const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const bool cacheable = dev >= 0 && dev < 64;
+  const unsigned long long bit = cacheable ? 1ull << dev : 0ull;
+  if (cacheable && (__atomic_load_n(done, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+  err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess && cacheable) __atomic_fetch_or(done, bit, __ATOMIC_RELEASE);
+  return err;
+}
+
 bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D,
-                            BshdStrides st, int box_heads, int box_rows) {
+                            BshdStrides st, int box_heads, int box_rows, bool use_cache) {
+  st = resolve_strides(st, S, heads, D);
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.base = base;
+  key.dims[0] = D;
+  key.dims[1] = heads;
+  key.dims[2] = S;
+  key.dims[3] = B;
+  key.strides[0] = st.h;
+  key.strides[1] = st.s;
+  key.strides[2] = st.b;
+  key.box_heads = box_heads;
+  key.box_rows = box_rows;
+  if (use_cache) {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    auto it = g_map_cache.find(key);
+    if (it != g_map_cache.end()) {
+      *map = it->second;
+      return true;
+    }
+  }
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  st = resolve_strides(st, S, heads, D);
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.h) * 2,
@@ -116,7 +231,12 @@ bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, in
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  if (!use_cache) return true;
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  if (g_map_cache.size() >= kMapCacheMax) g_map_cache.clear();
+  g_map_cache.emplace(key, *map);
+  return true;
 }
 
 }  // namespace fa
@@ -126,11 +246,11 @@ namespace {
 // Validates the arguments, then launches the kernel of `dtype` on `stream`.
 // `strides` (may be null: dense) holds the element strides along B, S, H of
 // q, k, v and out, in that order.
-fa_status_t forward(void* out, float* lse, const void* q, const void* k, const void* v, int B,
-                    int S, int H, int Hkv, int D, float scale, int mask_kind,
-                    int local_window_size, int dtype, void* stream,
-                    const fa::BshdStrides* strides) {
-  // ---- arguments (no CUDA call before these pass)
+// Argument checks of the no-cache forward (no CUDA call).
+fa_status_t check_forward_args(void* out, float* lse, const void* q, const void* k, const void* v,
+                               int B, int S, int H, int Hkv, int D, float scale, int mask_kind,
+                               int local_window_size, int dtype,
+                               const fa::BshdStrides* strides) {
   if (out == nullptr || q == nullptr || k == nullptr || v == nullptr)
     return fail(FA_ERR_INVALID_ARG, "null tensor pointer (out=%p q=%p k=%p v=%p)", out, q, k, v);
   if (B < 1 || S < 1 || H < 1 || Hkv < 1)
@@ -178,19 +298,25 @@ fa_status_t forward(void* out, float* lse, const void* q, const void* k, const v
                     names[t]);
     }
   }
+  return FA_OK;
+}
+
+fa_status_t forward(void* out, float* lse, const void* q, const void* k, const void* v, int B,
+                    int S, int H, int Hkv, int D, float scale, int mask_kind,
+                    int local_window_size, int dtype, void* stream,
+                    const fa::BshdStrides* strides) {
+  // ---- arguments (no CUDA call before these pass)
+  fa_status_t st = check_forward_args(out, lse, q, k, v, B, S, H, Hkv, D, scale, mask_kind,
+                                      local_window_size, dtype, strides);
+  if (st != FA_OK) return st;
 
   // ---- device
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
-  int major = 0, minor = 0;
-  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3)
-    return fail(FA_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+  if ((st = check_arch(dev)) != FA_OK) return st;
   unsigned* status = nullptr;
-  fa_status_t st = device_status_word(dev, &status);
-  if (st != FA_OK) return st;
+  if ((st = stream_status_word(dev, stream, &status)) != FA_OK) return st;
 
   fa::FwdProblem p;
   p.B = B;
@@ -207,6 +333,13 @@ fa_status_t forward(void* out, float* lse, const void* q, const void* k, const v
   p.status = status;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.stall_probe = g_stall_probe.load();
+  if (FA_TRACE) {
+    p.trace = g_trace_buf.load();
+    p.trace_ctas = p.trace != nullptr
+                       ? static_cast<long long>(g_trace_bytes.load() / fa::trace::kBytesPerCta)
+                       : 0;
+    p.lse_limit = g_lse_limit.load();
+  }
   if (strides != nullptr) {
     p.sq = strides[0];
     p.sk = strides[1];
@@ -352,12 +485,17 @@ KvPlan make_kv_plan(int B, int Sq, int S_cache, int H, int Hkv, int D, int causa
   return k;
 }
 
+// SM count of the current device (asked once per device).
 fa_status_t current_sm_count(int* out) {
+  static std::atomic<int> known[kMaxDevices];  // 0: not asked yet
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if (dev >= 0 && dev < kMaxDevices && (*out = known[dev].load(std::memory_order_acquire)) > 0)
+    return FA_OK;
   err = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return cuda_fail(err, "cudaDeviceGetAttribute(SM count)");
+  if (dev >= 0 && dev < kMaxDevices) known[dev].store(*out, std::memory_order_release);
   return FA_OK;
 }
 
@@ -431,14 +569,10 @@ fa_status_t fa_topk(float* values, int* indices, const float* scores, int B, int
   if (!aligned(values, 4) || !aligned(indices, 4) || !aligned(scores, 4) ||
       (workspace != nullptr && !aligned(workspace, 8)))
     return fail(FA_ERR_UNSUPPORTED, "buffers must be 4-byte aligned (workspace 8)");
-  int dev = 0;
+  int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
-  int major = 0, minor = 0, sms = 0;
-  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3)
-    return fail(FA_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+  if ((st = check_arch(dev)) != FA_OK) return st;
   if ((st = current_sm_count(&sms)) != FA_OK) return st;
   const TopkPlan t = make_topk_plan(B, V, K, sms);
   if (t.workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < t.workspace_bytes))
@@ -496,14 +630,10 @@ fa_status_t fa_mha_no_cache_f32_tc(float* out, float* lse, const float* q, const
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
-  int major = 0, minor = 0;
-  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3)
-    return fail(FA_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
-  unsigned* status = nullptr;
-  fa_status_t st = device_status_word(dev, &status);
+  fa_status_t st = check_arch(dev);
   if (st != FA_OK) return st;
+  unsigned* status = nullptr;
+  if ((st = stream_status_word(dev, stream, &status)) != FA_OK) return st;
   fa::F32x3Problem p{};
   p.B = B;
   p.S = S;
@@ -563,14 +693,10 @@ fa_status_t fa_mha_kv_cache(void* out, float* lse, const void* q, const void* k_
       (workspace != nullptr && !aligned(workspace, 16)))
     return fail(FA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned (lse, cache_lens: 4)");
 
-  int dev = 0;
+  int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
-  int major = 0, minor = 0, sms = 0;
-  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3)
-    return fail(FA_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+  if ((st = check_arch(dev)) != FA_OK) return st;
   if ((st = current_sm_count(&sms)) != FA_OK) return st;
   const KvPlan plan = make_kv_plan(B, Sq, S_cache, H, Hkv, D, mask_kind == FA_MASK_CAUSAL,
                                    local_window_size, num_splits, sms);
@@ -580,7 +706,7 @@ fa_status_t fa_mha_kv_cache(void* out, float* lse, const void* q, const void* k_
   if (static_cast<long long>(plan.splits) * Hkv * plan.n_ptiles * B > 0x7fffffffll)
     return fail(FA_ERR_UNSUPPORTED, "problem too large (grid)");
   unsigned* status = nullptr;
-  if ((st = device_status_word(dev, &status)) != FA_OK) return st;
+  if ((st = stream_status_word(dev, stream, &status)) != FA_OK) return st;
 
   fa::DecodeProblem p{};
   p.B = B;
@@ -640,6 +766,93 @@ fa_status_t fa_mha_no_cache_strided(void* out, float* lse, const void* q, const 
                  stream, st);
 }
 
+// Device workspace of fa_mha_no_cache_host: q, k, v, out, lse, then (fp32
+// with D 64 or 128) the tensor-core path's bf16 planes, each 256-byte aligned.
+struct HostLayout {
+  unsigned long long q, k, v, out, lse, planes, total;
+};
+HostLayout host_layout(int B, int S, int H, int Hkv, int D, int dtype) {
+  const unsigned long long e = dtype == FA_DTYPE_BF16 ? 2ull : 4ull;
+  const unsigned long long q_bytes = static_cast<unsigned long long>(B) * S * H * D * e;
+  const unsigned long long kv_bytes = static_cast<unsigned long long>(B) * S * Hkv * D * e;
+  const unsigned long long lse_bytes = static_cast<unsigned long long>(B) * H * S * 4ull;
+  HostLayout l{};
+  l.q = 0;
+  l.k = align256(l.q + q_bytes);
+  l.v = align256(l.k + kv_bytes);
+  l.out = align256(l.v + kv_bytes);
+  l.lse = align256(l.out + q_bytes);
+  l.planes = align256(l.lse + lse_bytes);
+  const bool f32_tc = dtype == FA_DTYPE_F32 && (D == 64 || D == 128);
+  l.total = l.planes + (f32_tc ? fa::f32x3_workspace_bytes(B, S, Hkv, D) : 0ull);
+  return l;
+}
+
+unsigned long long fa_mha_no_cache_host_workspace(int B, int S, int H, int Hkv, int D,
+                                                  int dtype) {
+  if (B < 1 || S < 1 || H < 1 || Hkv < 1 || D < 1 ||
+      (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F32))
+    return 0ull;
+  return host_layout(B, S, H, Hkv, D, dtype).total;
+}
+
+fa_status_t fa_mha_no_cache_host(void* out, float* lse, const void* q, const void* k,
+                                 const void* v, int B, int S, int H, int Hkv, int D, float scale,
+                                 int mask_kind, int local_window_size, int dtype, void* workspace,
+                                 unsigned long long workspace_bytes, void* stream) {
+  if (out == nullptr || q == nullptr || k == nullptr || v == nullptr)
+    return fail(FA_ERR_INVALID_ARG, "null host pointer (out=%p q=%p k=%p v=%p)", out, q, k, v);
+  if (workspace == nullptr || !aligned(workspace, 256))
+    return fail(FA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device buffer");
+  char* ws = static_cast<char*>(workspace);
+  fa_status_t st = FA_OK;
+  if (B >= 1 && S >= 1 && H >= 1 && Hkv >= 1 && D >= 1) {
+    const HostLayout l = host_layout(B, S, H, Hkv, D, dtype);
+    // The device-side arguments the launch will get (checked before any copy).
+    st = check_forward_args(ws + l.out, lse != nullptr ? reinterpret_cast<float*>(ws + l.lse)
+                                                       : nullptr,
+                            ws + l.q, ws + l.k, ws + l.v, B, S, H, Hkv, D, scale, mask_kind,
+                            local_window_size, dtype, nullptr);
+    if (st == FA_OK && workspace_bytes < l.total)
+      st = fail(FA_ERR_INVALID_ARG, "workspace of %llu bytes needed, %llu given", l.total,
+                workspace_bytes);
+  } else {
+    st = check_forward_args(out, lse, q, k, v, B, S, H, Hkv, D, scale, mask_kind,
+                            local_window_size, dtype, nullptr);
+  }
+  if (st != FA_OK) return st;
+  const HostLayout l = host_layout(B, S, H, Hkv, D, dtype);
+  const unsigned long long e = dtype == FA_DTYPE_BF16 ? 2ull : 4ull;
+  const unsigned long long q_bytes = static_cast<unsigned long long>(B) * S * H * D * e;
+  const unsigned long long kv_bytes = static_cast<unsigned long long>(B) * S * Hkv * D * e;
+  const unsigned long long lse_bytes = static_cast<unsigned long long>(B) * H * S * 4ull;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if ((err = cudaMemcpyAsync(ws + l.q, q, q_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (err = cudaMemcpyAsync(ws + l.k, k, kv_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (err = cudaMemcpyAsync(ws + l.v, v, kv_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(err, "cudaMemcpyAsync (inputs to the device)");
+  float* lse_d = lse != nullptr ? reinterpret_cast<float*>(ws + l.lse) : nullptr;
+  if (dtype == FA_DTYPE_F32 && (D == 64 || D == 128)) {
+    st = fa_mha_no_cache_f32_tc(reinterpret_cast<float*>(ws + l.out), lse_d,
+                                reinterpret_cast<const float*>(ws + l.q),
+                                reinterpret_cast<const float*>(ws + l.k),
+                                reinterpret_cast<const float*>(ws + l.v), B, S, H, Hkv, D, scale,
+                                mask_kind, local_window_size, ws + l.planes,
+                                l.total - l.planes, stream);
+  } else {
+    st = forward(ws + l.out, lse_d, ws + l.q, ws + l.k, ws + l.v, B, S, H, Hkv, D, scale,
+                 mask_kind, local_window_size, dtype, stream, nullptr);
+  }
+  if (st != FA_OK) return st;
+  if ((err = cudaMemcpyAsync(out, ws + l.out, q_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(err, "cudaMemcpyAsync (output to the host)");
+  if (lse != nullptr &&
+      (err = cudaMemcpyAsync(lse, lse_d, lse_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(err, "cudaMemcpyAsync (lse to the host)");
+  return FA_OK;
+}
+
 fa_status_t fa_device_status(int device, int clear) {
   if (device < 0 || device >= kMaxDevices)
     return fail(FA_ERR_INVALID_ARG, "device index %d", device);
@@ -653,26 +866,86 @@ fa_status_t fa_device_status(int device, int clear) {
   if (err != cudaSuccess) {
     result = cuda_fail(err, "cudaDeviceSynchronize");
   } else {
-    unsigned* word = nullptr;
-    {
-      std::lock_guard<std::mutex> lock(g_mutex);
-      word = g_status[device];
-    }
-    if (word != nullptr) {
-      unsigned value = 0;
-      err = cudaMemcpy(&value, word, sizeof(value), cudaMemcpyDeviceToHost);
+    // The lock keeps fa_shutdown from freeing the words while they are read.
+    std::lock_guard<std::mutex> lock(g_mutex);
+    unsigned* words = g_pool[device].words;
+    if (words != nullptr) {
+      static unsigned host[kStatusSlots];
+      err = cudaMemcpy(host, words, sizeof(host), cudaMemcpyDeviceToHost);
       if (err != cudaSuccess) {
-        result = cuda_fail(err, "cudaMemcpy(status word)");
+        result = cuda_fail(err, "cudaMemcpy(status words)");
       } else {
-        if (clear && value != 0 && (err = cudaMemset(word, 0, sizeof(unsigned))) != cudaSuccess)
-          result = cuda_fail(err, "cudaMemset(status word)");
-        else if (value & fa::kStatusWaitTimeout)
-          result = fail(FA_ERR_TIMEOUT, "a kernel on device %d gave up on a bounded wait", device);
+        unsigned bits = 0;
+        for (int i = 0; i < kStatusSlots; ++i) bits |= host[i];
+        if (clear && bits != 0 &&
+            (err = cudaMemset(words, 0, kStatusSlots * sizeof(unsigned))) != cudaSuccess)
+          result = cuda_fail(err, "cudaMemset(status words)");
+        else if (clear && bits != 0 && (err = cudaDeviceSynchronize()) != cudaSuccess)
+          result = cuda_fail(err, "cudaDeviceSynchronize");
+        else
+          result = status_from_bits(bits, "the device");
       }
     }
   }
   if (prev != device) cudaSetDevice(prev);
   return result;
+}
+
+fa_status_t fa_stream_status(void* stream, int clear) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned* word = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    StatusPool& pool = g_pool[dev];
+    if (pool.words != nullptr) {
+      auto it = pool.slot_of.find(stream);
+      if (it != pool.slot_of.end())
+        word = pool.words + it->second;
+      else if (static_cast<int>(pool.slot_of.size()) >= kStatusSlots - 1)
+        word = pool.words + (kStatusSlots - 1);
+    }
+  }
+  unsigned bits = 0;
+  if (word != nullptr) {
+    err = cudaMemcpyAsync(&bits, word, sizeof(bits), cudaMemcpyDeviceToHost, s);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaMemcpyAsync(status word)");
+    if (clear && (err = cudaMemsetAsync(word, 0, sizeof(unsigned), s)) != cudaSuccess)
+      return cuda_fail(err, "cudaMemsetAsync(status word)");
+  }
+  err = cudaStreamSynchronize(s);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaStreamSynchronize");
+  return status_from_bits(bits, "this stream");
+}
+
+fa_status_t fa_trace_set_buffer(void* buf, unsigned long long bytes) {
+  if (!FA_TRACE) {
+    if (buf == nullptr) return FA_OK;
+    return fail(FA_ERR_UNSUPPORTED, "event traces need the debug build (libfa_mha_debug.so)");
+  }
+  if (buf != nullptr && (reinterpret_cast<uintptr_t>(buf) % 16 != 0))
+    return fail(FA_ERR_INVALID_ARG, "trace buffer must be 16-byte aligned");
+  g_trace_buf.store(nullptr);
+  g_trace_bytes.store(buf != nullptr ? bytes : 0ull);
+  g_trace_buf.store(buf);
+  return FA_OK;
+}
+
+unsigned long long fa_trace_bytes_per_cta(void) { return FA_TRACE ? fa::trace::kBytesPerCta : 0ull; }
+
+long long fa_trace_ctas(int B, int S, int H, int D) {
+  if (B < 1 || S < 1 || H < 1 || D < 8 || D > 128) return 0;
+  return static_cast<long long>(fa::fwd_bf16_tc_ctas(S)) * H * B;
+}
+
+fa_status_t fa_debug_set_lse_limit(long long elems) {
+  if (!FA_TRACE) return fail(FA_ERR_UNSUPPORTED, "bounds guards need the debug build");
+  if (elems < 0) return fail(FA_ERR_INVALID_ARG, "limit must be >= 0");
+  g_lse_limit.store(elems);
+  return FA_OK;
 }
 
 unsigned long long fa_set_wait_timeout_ns(unsigned long long ns) {
@@ -681,13 +954,14 @@ unsigned long long fa_set_wait_timeout_ns(unsigned long long ns) {
 
 int fa_set_stall_probe(int enable) { return g_stall_probe.exchange(enable ? 1 : 0); }
 
-const char* fa_status_string(int status) {
+const char* fa_status_string(fa_status_t status) {
   switch (status) {
     case FA_OK: return "FA_OK";
     case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
     case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_BOUNDS: return "FA_ERR_BOUNDS";
     default: return "FA_ERR_UNKNOWN";
   }
 }
@@ -697,16 +971,22 @@ const char* fa_last_error_message(void) { return t_message; }
 int fa_version(void) { return kVersion; }
 
 void fa_shutdown(void) {
-  std::lock_guard<std::mutex> lock(g_mutex);
-  int prev = -1;
-  cudaGetDevice(&prev);
-  for (int d = 0; d < kMaxDevices; ++d) {
-    if (g_status[d] != nullptr) {
-      if (cudaSetDevice(d) == cudaSuccess) cudaFree(g_status[d]);
-      g_status[d] = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int prev = -1;
+    cudaGetDevice(&prev);
+    for (int d = 0; d < kMaxDevices; ++d) {
+      StatusPool& pool = g_pool[d];
+      if (pool.words != nullptr) {
+        if (cudaSetDevice(d) == cudaSuccess) cudaFree(pool.words);
+        pool.words = nullptr;
+      }
+      pool.slot_of.clear();
     }
+    if (prev >= 0) cudaSetDevice(prev);
   }
-  if (prev >= 0) cudaSetDevice(prev);
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  g_map_cache.clear();
 }
 
 }  // extern "C"

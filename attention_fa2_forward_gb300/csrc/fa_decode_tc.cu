@@ -613,9 +613,10 @@ cudaError_t launch_d(const DecodeProblem& p, void* out, const void* q, const voi
     return cudaErrorInvalidValue;
   const long long grid = static_cast<long long>(p.splits) * p.Hkv * p.n_ptiles * p.B;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  cudaError_t err = cudaFuncSetAttribute(fa_decode_bf16_tc_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DCfg<D>::kSmemBytes);
+  static unsigned long long attr_done = 0;
+  cudaError_t err = ensure_smem_attr(&attr_done, reinterpret_cast<const void*>(
+                                                     &fa_decode_bf16_tc_kernel<D>),
+                                     DCfg<D>::kSmemBytes);
   if (err != cudaSuccess) return err;
   fa_decode_bf16_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, DCfg<D>::kSmemBytes,
                                 stream>>>(tq, tk, tv, to, p);

@@ -541,8 +541,9 @@ cudaError_t launch_d(const F32x3Problem& p, cudaStream_t stream) {
   const int nqb = (p.S + kBM - 1) / kBM;
   const long long grid = static_cast<long long>(nqb) * p.H * p.B;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(fa_fwd_f32x3_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             X3Cfg<D>::kSmemBytes);
+  static unsigned long long attr_done = 0;
+  err = ensure_smem_attr(&attr_done, reinterpret_cast<const void*>(&fa_fwd_f32x3_kernel<D>),
+                         X3Cfg<D>::kSmemBytes);
   if (err != cudaSuccess) return err;
   fa_fwd_f32x3_kernel<D><<<static_cast<unsigned>(grid), kThreads, X3Cfg<D>::kSmemBytes, stream>>>(
       tk[0], tk[1], tk[2], tv[0], tv[1], tv[2], p, nqb);

@@ -33,6 +33,9 @@
 // on time-out the CTA records kStatusWaitTimeout in the status word, stops
 // issuing work, waits (again bounded) for its own copies and MMAs in flight,
 // releases its tensor memory and returns.
+//
+// The debug build (FA_TRACE=1) adds the event trace and bounds guards of
+// fa_trace.cuh; in the default build both compile to nothing.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -40,6 +43,7 @@
 
 #include "fa_internal.h"
 #include "fa_tile.cuh"
+#include "fa_trace.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -114,6 +118,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  namespace tr = trace;
+  const int trace_role = warp == kLoadWarp ? tr::kRoleProducer
+                         : warp == kMmaWarp ? tr::kRoleMma
+                                            : tr::kRoleSoftmax0 + (warp >> 2);
+  tr::Recorder rec(p.trace, p.trace_ctas, trace_role,
+                   lane == 0 && (warp >= kSoftmaxWarps || (warp & 3) == 0));
+  if (warp == kLoadWarp) rec(tr::kCtaStart, tr::sm_id());
 
   // ---- work item: heaviest (last) query blocks first
   const int per_qb = p.H * p.B;
@@ -194,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int bx = 0; bx < C::kBoxes; ++bx)
             ptx::tma_load_4d(sQ + t * C::kTileBytes + bx * kBoxBytes, &tm_q, bar_q_full + 8 * t,
                              bx * 64, h, q0[t], b, pol_q);
+          rec(tr::kQLoadIssued, t);
         }
       }
       uint32_t armed = 0, armed_parity = 0;  // per slot: bit set once loaded / last parity
@@ -209,12 +221,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // A tile starting past the last key would be a planning error.
+          tr::guard(j * kBN < p.S, p.status, kStatusBoundsGuard);
           ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * s, C::kTileBytes);
           const CUtensorMap* tm = kind == 0 ? &tm_k : &tm_v;
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx)
             ptx::tma_load_4d(sKV + s * C::kTileBytes + bx * kBoxBytes, tm, bar_kv_full + 8 * s,
                              bx * 64, hk, j * kBN, b, pol_kv);
+          rec(kind == 0 ? tr::kKLoadIssued : tr::kVLoadIssued, j);
           armed |= 1u << s;
           armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
         }
@@ -244,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fail();
           ok = false;
         }
+      rec(tr::kQReady, 0);
       auto in_tile = [&](int t, int j) { return j >= lo[t] && j < hi[t]; };
       // Wait for ring entry idx; returns its slot or -1 on time-out.
       auto wait_kv = [&](int idx) -> int {
@@ -259,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq0 = ptx::smem_desc_sw128(sQ, 16, 1024);
       const uint64_t dk0 = ptx::smem_desc_sw128(sKV, 16, 1024);
       const uint64_t dv0 = ptx::smem_desc_sw128(sKV, kBoxBytes, 1024);
-      auto issue_s = [&](int t, int kslot) {
+      auto issue_s = [&](int t, int kslot, int j) {
         const uint64_t dq = dq0 + static_cast<uint32_t>((t * C::kTileBytes) >> 4);
         const uint64_t dk = dk0 + static_cast<uint32_t>((kslot * C::kTileBytes) >> 4);
 #pragma unroll
@@ -268,14 +284,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_ss(tmem + t * kBN, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
         }
         ptx::tc_commit(bar_s_full + 8 * t);
+        rec(tr::kSIssued, (t << 16) | j);
       };
-      auto issue_pv = [&](int t, int vslot, bool accumulate) {
+      auto issue_pv = [&](int t, int vslot, bool accumulate, int j) {
         const uint64_t dv = dv0 + static_cast<uint32_t>((vslot * C::kTileBytes) >> 4);
         const uint32_t acc = accumulate ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           ptx::mma_ts(tmem + C::kColO + t * D, tmem + t * kBN + kk * 8,
                       dv + static_cast<uint32_t>(kk * 128), kIdescPV, kk > 0 ? 1u : acc);
+        rec(tr::kPvIssued, (t << 16) | j);
       };
       uint32_t p_phase[kQTiles] = {0u, 0u};
       auto wait_p = [&](int t) -> bool {
@@ -295,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int t = 0; t < kQTiles; ++t)
-            if (in_tile(t, jlo)) issue_s(t, ks);
+            if (in_tile(t, jlo)) issue_s(t, ks, jlo);
           ptx::tc_commit(bar_kv_empty + 8 * ks);
         }
       }
@@ -305,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (vs < 0) break;
         if (in_tile(0, j)) {
           if (!wait_p(0)) break;
-          issue_pv(0, vs, j > lo[0]);
+          issue_pv(0, vs, j > lo[0], j);
           if (j == hi[0] - 1) ptx::tc_commit(bar_o_full);
         }
         const bool has_next = j + 1 < jhi;
@@ -313,22 +331,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (has_next) {
           ks = wait_kv(2 * rel + 2);
           if (ks < 0) break;
-          if (in_tile(0, j + 1)) issue_s(0, ks);
+          if (in_tile(0, j + 1)) issue_s(0, ks, j + 1);
         }
         if (in_tile(1, j)) {
           if (!wait_p(1)) break;
-          issue_pv(1, vs, j > lo[1]);
+          issue_pv(1, vs, j > lo[1], j);
           if (j == hi[1] - 1) ptx::tc_commit(bar_o_full + 8);
         }
         ptx::tc_commit(bar_kv_empty + 8 * vs);
         if (has_next) {
-          if (in_tile(1, j + 1)) issue_s(1, ks);
+          if (in_tile(1, j + 1)) issue_s(1, ks, j + 1);
           ptx::tc_commit(bar_kv_empty + 8 * ks);
         }
       }
       // Every MMA must have finished before tensor memory is released.
       ptx::tc_commit(bar_drain);
       ptx::mbar_wait(bar_drain, 0, drain_limit);
+      rec(tr::kMmaDrained, 0);
     }
     __syncwarp();
   } else {
@@ -365,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
+      rec(tr::kSReady, j);
 
       uint32_t r[kBN];
 #pragma unroll
@@ -425,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar_p_full + 8 * t);
+      rec(tr::kPReady, j | (rescale ? 1u << 23 : 0u));
     }
 
     // ---- epilogue: O / l -> bf16 -> shared (swizzled) -> TMA store; LSE.
@@ -437,8 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
       }
     }
-    const bool do_store = ok && has_work;
+    // A store of rows that start past S would be a planning error.
+    const bool do_store = ok && has_work && tr::guard(tq0 < p.S, p.status, kStatusBoundsGuard);
     if (do_store) {
+      rec(tr::kEpilogueStart, 0);
       ptx::tc_fence_after();
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
@@ -462,8 +485,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (do_store && p.lse != nullptr && i < p.S) {
       const float m_fin = m_use == -INFINITY ? 0.f : m_use;
-      p.lse[(static_cast<size_t>(b) * p.H + h) * p.S + i] = (m_fin + __log2f(l_run)) * kLn2;
+      const long long idx = (static_cast<long long>(b) * p.H + h) * p.S + i;
+      const long long lse_limit =
+          p.lse_limit > 0 ? p.lse_limit : static_cast<long long>(p.B) * p.H * p.S;
+      if (tr::guard(idx < lse_limit, p.status, kStatusBoundsGuard))
+        p.lse[idx] = (m_fin + __log2f(l_run)) * kLn2;
     }
+    if (do_store) rec(tr::kEpilogueEnd, 0);
   }
 
   ptx::tc_fence_before();
@@ -481,17 +509,18 @@ cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* 
   // The maps carry the real head dim p.D <= D: loads zero-fill columns
   // p.D..D-1 (adding nothing to Q K^T and giving zero O columns) and the
   // store clips them.
-  if (!encode_bshd_tensor_map(&tq, q, p.B, p.S, p.H, p.D, p.sq) ||
-      !encode_bshd_tensor_map(&tk, k, p.B, p.S, p.Hkv, p.D, p.sk) ||
-      !encode_bshd_tensor_map(&tv, v, p.B, p.S, p.Hkv, p.D, p.sv) ||
-      !encode_bshd_tensor_map(&to, out, p.B, p.S, p.H, p.D, p.so))
+  if (!encode_bshd_tensor_map(&tq, q, p.B, p.S, p.H, p.D, p.sq, 1, kBM, p.cache_maps) ||
+      !encode_bshd_tensor_map(&tk, k, p.B, p.S, p.Hkv, p.D, p.sk, 1, kBN, p.cache_maps) ||
+      !encode_bshd_tensor_map(&tv, v, p.B, p.S, p.Hkv, p.D, p.sv, 1, kBN, p.cache_maps) ||
+      !encode_bshd_tensor_map(&to, out, p.B, p.S, p.H, p.D, p.so, 1, kBM, p.cache_maps))
     return cudaErrorInvalidValue;
   const int nqb = (p.S + kQTiles * kBM - 1) / (kQTiles * kBM);
   const long long grid = static_cast<long long>(nqb) * p.H * p.B;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  cudaError_t err = cudaFuncSetAttribute(fa_fwd_bf16_tc_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<D>::kSmemBytes);
+  static unsigned long long attr_done = 0;
+  cudaError_t err = ensure_smem_attr(&attr_done, reinterpret_cast<const void*>(
+                                                     &fa_fwd_bf16_tc_kernel<D>),
+                                     Cfg<D>::kSmemBytes);
   if (err != cudaSuccess) return err;
   fa_fwd_bf16_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(
       tq, tk, tv, to, p, nqb);
@@ -499,6 +528,8 @@ cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* 
 }
 
 }  // namespace
+
+int fwd_bf16_tc_ctas(int S) { return (S + kQTiles * kBM - 1) / (kQTiles * kBM); }
 
 cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, const void* k,
                                const void* v, cudaStream_t stream) {

@@ -9,8 +9,9 @@
 
 namespace fa {
 
-// Bits of the per-device status word the kernels may set.
+// Bits of the status word the kernels may set.
 constexpr unsigned kStatusWaitTimeout = 1u;
+constexpr unsigned kStatusBoundsGuard = 2u;  // debug build: a bounds guard skipped an access
 
 // Element strides of a BSHD (or BShD) view along B, S and H; D is
 // contiguous. All zero means the dense layout of the view's shape.
@@ -40,6 +41,10 @@ struct FwdProblem {
   unsigned long long wait_limit_ns;
   int stall_probe;       // test hook: the MMA issuer first waits on a barrier nothing signals
   BshdStrides sq, sk, sv, so;  // layouts of q, k, v, out (zero: dense)
+  void* trace = nullptr;       // debug build: event records (fa_trace.cuh), or nullptr
+  long long trace_ctas = 0;    // CTAs the trace buffer has room for
+  long long lse_limit = 0;     // debug build: LSE elements a guard lets the kernel write
+  bool cache_maps = true;      // false: encode the tensor maps without the (allocating) cache
 };
 
 // Attention over a KV cache (bf16, tensor cores): batch b holds L_b keys at
@@ -71,6 +76,8 @@ cudaError_t launch_decode_bf16_tc(const DecodeProblem& p, void* out, const void*
 // 16-byte-aligned dense BSHD / BShD bf16 tensors. Returns a cudaError_t.
 cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, const void* k,
                                const void* v, cudaStream_t stream);
+// Query blocks (CTAs per (batch, head)) of that kernel for S queries.
+int fwd_bf16_tc_ctas(int S);
 
 // CUDA-core fp32 forward for fp32 tensors.
 cudaError_t launch_fwd_f32_simt(const FwdProblem& p, float* out, const float* q, const float* k,
@@ -118,10 +125,24 @@ cudaError_t launch_topk(const TopkProblem& p, cudaStream_t stream);
 // Stores `msg` as the calling thread's fa_last_error_message().
 void record_error_message(const char* msg);
 
+// The bounded-wait limit every launch uses (fa_set_wait_timeout_ns).
+unsigned long long wait_limit_ns();
+
+// Raises `func`'s dynamic shared-memory limit to `bytes` once per device:
+// `done` (one per kernel, zero-initialised static) keeps a bit per device
+// index that has been set up. Later calls on that device cost one
+// cudaGetDevice.
+cudaError_t ensure_smem_attr(unsigned long long* done, const void* func, int bytes);
+
 // Encodes a 4-D BSHD tensor map (dims D, heads, S, B; element strides `st`,
 // D contiguous) for bf16 data with a {64, box_heads, box_rows, 1} box and
-// 128-byte swizzle. Returns false on failure.
+// 128-byte swizzle. Returns false on failure. Maps are cached, keyed on every
+// argument (address, sizes, strides, box): a repeated call copies the cached
+// map instead of encoding it again; fa_shutdown() empties the cache. With
+// use_cache false the map is encoded and the cache neither read nor grown
+// (no host allocation).
 bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D,
-                            BshdStrides st, int box_heads = 1, int box_rows = 128);
+                            BshdStrides st, int box_heads = 1, int box_rows = 128,
+                            bool use_cache = true);
 
 }  // namespace fa

@@ -31,7 +31,6 @@ constexpr size_t kNoAllocScratchBytes = 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
@@ -136,8 +135,9 @@ extern "C" fa_status_t fa_mha_no_cache_noalloc(void* out, float* lse, const void
   p.scale_log2 = scale * 1.4426950408889634f;
   p.lse = lse;
   p.status = status;
-  p.wait_limit_ns = kWaitLimitNs;
+  p.wait_limit_ns = fa::wait_limit_ns();  // the limit fa_set_wait_timeout_ns sets
   p.stall_probe = 0;
+  p.cache_maps = false;  // the tensor-map cache grows a host hash table
   err = fa::launch_fwd_bf16_tc(p, out, q, k, v, s);
   if (err != cudaSuccess)
     return noalloc_fail(FA_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(err));

@@ -14,14 +14,6 @@ namespace tile {
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr uint32_t kNegInfBits = 0xff800000u;
 
-// Pairs of score columns whose exponential runs on the FMA pipe (a degree-3
-// polynomial) instead of the MUFU unit: kPolyPer8 of every 8 pairs, spread
-// evenly. At 0 every exponential uses ex2.approx.
-constexpr int kPolyPer8 = 0;
-__host__ __device__ constexpr bool poly_pair(int i) {
-  return ((i & 7) * kPolyPer8) / 8 != (((i & 7) + 1) * kPolyPer8) / 8;
-}
-
 // Hides (-inf) the scores outside the visible key columns [vlo, vhi] of the
 // tile; with a zero scale the visible ones become 0 (the caller then uses 1
 // as the multiplier, which keeps -inf * 0 out of the hidden lanes).
@@ -64,12 +56,8 @@ __device__ __forceinline__ float exp2_to_bf16(uint32_t* r, float ce, float neg_b
   for (int i = 0; i < kBN / 2; ++i) {
     uint32_t lo, hi;
     ptx::unpair(ptx::fma2(ptx::pair(r[2 * i], r[2 * i + 1]), c2, nb2), lo, hi);
-    if (poly_pair(i)) {
-      ptx::exp2_poly3_pair(lo, hi);
-    } else {
-      lo = __float_as_uint(ptx::ex2_approx(__uint_as_float(lo)));
-      hi = __float_as_uint(ptx::ex2_approx(__uint_as_float(hi)));
-    }
+    lo = __float_as_uint(ptx::ex2_approx(__uint_as_float(lo)));
+    hi = __float_as_uint(ptx::ex2_approx(__uint_as_float(hi)));
     const uint64_t pp = ptx::pair(lo, hi);
     if ((i & 3) == 0) acc0 = ptx::add2(acc0, pp);
     if ((i & 3) == 1) acc1 = ptx::add2(acc1, pp);

@@ -268,40 +268,6 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
-// 2^x on the FMA pipe for a pair of fp32 values (bit patterns in/out), for
-// x <= 126 (x below -126 is clamped there and returns ~1e-38 instead of 0).
-// Cody-Waite style range reduction x = n + f with n = round(x) and
-// f in [-1/2, 1/2]: adding 1.5 * 2^23 leaves n in the low mantissa bits, and
-// n << 23 added to the bits of 2^f scales by 2^n. 2^f is a degree-3 minimax
-// polynomial in relative error fitted on [-1/2, 1/2] (Remez exchange; maximum
-// relative error 7.5e-5 in fp32 arithmetic, see fit_exp2_poly.py).
-__device__ __forceinline__ void exp2_poly3_pair(uint32_t& lo, uint32_t& hi) {
-  const float xl = fmaxf(__uint_as_float(lo), -126.f);
-  const float xh = fmaxf(__uint_as_float(hi), -126.f);
-  const uint64_t x = pair(__float_as_uint(xl), __float_as_uint(xh));
-  const uint64_t magic = pair(0x4B400000u, 0x4B400000u);  // 1.5 * 2^23
-  const uint64_t t = add2(x, magic);
-  const uint64_t f = sub2(x, sub2(t, magic));
-  const uint64_t c0 = pair(0x3F7FFB49u, 0x3F7FFB49u);  // 0.99992806
-  const uint64_t c1 = pair(0x3F31798Du, 0x3F31798Du);  // 0.69326097
-  const uint64_t c2 = pair(0x3E786F0Du, 0x3E786F0Du);  // 0.24261113
-  const uint64_t c3 = pair(0x3D61FBB0u, 0x3D61FBB0u);  // 0.05517167
-  uint64_t p = fma2(c3, f, c2);
-  p = fma2(p, f, c1);
-  p = fma2(p, f, c0);
-  uint32_t pl, ph, tl, th;
-  unpair(p, pl, ph);
-  unpair(t, tl, th);
-  lo = pl + (tl << 23);
-  hi = ph + (th << 23);
-}
-
 // Two fp32 values -> bf16x2 (round to nearest even); `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

@@ -698,9 +698,15 @@ cudaError_t launch_topk(const TopkProblem& p, cudaStream_t stream) {
                      2048) <= 228 * 1024,
                 "two chunk CTAs share an SM up to the largest clustered K");
   static_assert(kTopkMaxCluster * kMaxTopK <= kRingKeys, "a cluster's candidates fit the ring");
-  auto launch = [&](auto kernel) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(csmem));
+  static_assert(kWarps * kRing * kWarpStep * 4 + kWarps * (kMaxTopK + kWarpStep) * 8 +
+                        kWarps * 256 * 4 + kWarps * kMaxTopK * 8 <= 227 * 1024,
+                "the largest K's chunk CTA fits the shared-memory limit");
+  // Each kernel's shared-memory limit is raised once per device, to what the
+  // largest K needs.
+  static unsigned long long attr_done[2] = {0, 0};
+  auto launch = [&](auto kernel, int which) -> cudaError_t {
+    cudaError_t e = ensure_smem_attr(&attr_done[which], reinterpret_cast<const void*>(kernel),
+                                     static_cast<int>(chunk_smem_bytes(kMaxTopK)));
     if (e != cudaSuccess) return e;
     uint32_t* vals = reinterpret_cast<uint32_t*>(p.values);
     if (!clustered) {
@@ -723,15 +729,16 @@ cudaError_t launch_topk(const TopkProblem& p, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kernel, p.scores, p.row_stride, p.V, p.K, p.chunk,
                               p.n_chunks, p.cand, vals, p.indices, 1);
   };
-  cudaError_t err = vec ? launch(topk_chunk_kernel<true>) : launch(topk_chunk_kernel<false>);
+  cudaError_t err = vec ? launch(topk_chunk_kernel<true>, 1) : launch(topk_chunk_kernel<false>, 0);
   if (err != cudaSuccess) return err;
   err = cudaGetLastError();
   if (err != cudaSuccess || p.n_chunks == 1 || clustered) return err;  // rows already finished
   int P = 1;
   while (P < p.K) P <<= 1;
   const size_t smem = (static_cast<size_t>(p.n_chunks) * p.K + P) * sizeof(uint64_t);
-  err = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+  static unsigned long long merge_attr_done = 0;
+  err = ensure_smem_attr(&merge_attr_done, reinterpret_cast<const void*>(&topk_merge_kernel),
+                         static_cast<int>((kMaxTopkCandidates + kMaxTopK) * sizeof(uint64_t)));
   if (err != cudaSuccess) return err;
   topk_merge_kernel<<<p.B, kThreads, smem, stream>>>(
       p.cand, p.n_chunks, p.K, reinterpret_cast<uint32_t*>(p.values), p.indices);

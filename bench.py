@@ -2,8 +2,10 @@
 
 One step = one forward pass of the whole hot path (one kernel launch) over
 one batch of the workload's synthetic inputs, resident in HBM. L2 is flushed
-(a 256 MiB buffer is rewritten) before every timed step and each step's
-kernel is timed with CUDA events on the launching stream.
+before every timed step (a 256 MiB buffer is rewritten, then another 256 MiB
+buffer is read so that no dirty line is left to be written back inside the
+timed step) and each step's kernel is timed with CUDA events on the
+launching stream.
 
 Prints ONE JSON line (rank 0). Metric: attention forward TFLOP/s counting
 only unmasked (query, key) pairs, FLOPs = 4 * B * H * D * pairs.
@@ -45,6 +47,8 @@ L2_BYTES = 129 << 20  # GB300 L2 (about 129 MB)
 # number includes).
 SPIN_CYCLES = 200_000
 KERNEL_NAME = "fa_fwd_bf16_tc_kernel"
+# Workloads whose oracle figure is also taken on one host thread.
+SINGLE_THREAD_WORKLOADS = ("tiny_f32", "mha_s1024_d64", "gqa_s4096_d128")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -169,48 +173,6 @@ def profiled_traffic(workload: str, kernel: str = KERNEL_NAME,
 
 
 # ----------------------------------------------------------------- end to end
-def pipelined_e2e_ms(n_steps, copy_in, compute, copy_out, stream):
-    """Milliseconds per step of n_steps end-to-end steps over two buffer sets
-    (slot = step % 2): step i's inputs are copied in on one stream while step
-    i - 1 computes, and its result is copied out on a third. Events keep a
-    slot's inputs from being overwritten before its kernel has read them and
-    its output before it has been copied out. The timed region runs from
-    before step 0's first copy to after the last step's copy out.
-    copy_in(slot) / compute(slot) / copy_out(slot) enqueue on the current
-    stream."""
-    import torch
-
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = lambda: torch.cuda.Event()
-    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    s_in.wait_event(e0)
-    for i in range(n_steps):
-        sl = i % 2
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(comp_done[sl])
-            copy_in(sl)
-            in_done[sl].record(s_in)
-        with torch.cuda.stream(stream):
-            stream.wait_event(in_done[sl])
-            if i >= 2:
-                stream.wait_event(out_done[sl])
-            compute(sl)
-            comp_done[sl].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(comp_done[sl])
-            copy_out(sl)
-            out_done[sl].record(s_out)
-    for sl in range(min(2, n_steps)):
-        stream.wait_event(out_done[sl])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / n_steps
-
-
 def prefill_traffic(w):
     """Profiled DRAM bytes per launch of the kernel that serves workload w:
     the bf16 tensor-core kernel up to D = 128, the one-Q-tile kernel above, the
@@ -289,6 +251,48 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
                 "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------- L2 flush
+class L2Flush:
+    """Between timed steps: write a buffer larger than L2 (evicting the
+    inputs), then read a second one, so the write's dirty lines are written
+    back before the step instead of during it. Outside the timed region."""
+
+    NOTE = ("flushed before every step: 256 MiB written, then another 256 MiB read (L2 holds "
+            "no input and no dirty line when the step starts)")
+
+    def __init__(self, device, enabled: bool = True):
+        import torch
+        n = L2_FLUSH_BYTES // 4 if enabled else 0
+        self.w = torch.empty(n, dtype=torch.float32, device=device)
+        self.r = torch.ones(n, dtype=torch.float32, device=device)
+        self.enabled = enabled
+
+    def __call__(self):
+        if self.enabled:
+            self.w.zero_()
+            self.sink = self.r.sum()
+
+
+def step_stats(kernel_ms):
+    """Mean and median of per-step times (ms)."""
+    return statistics.fmean(kernel_ms), statistics.median(kernel_ms)
+
+
+def host_cost_us(call, n: int = 200):
+    """Host microseconds per call of `call` (which enqueues GPU work and does
+    not synchronise), averaged over n calls after a warm-up."""
+    import torch
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        call()
+    dt = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    return dt / n * 1e6
 
 
 # ----------------------------------------------------------------- distributed
@@ -394,20 +398,26 @@ def bench_ours(args, w, world, rank, local, dist):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    fa.load_library()
+    lib = fa.load_library()
     q_h, k_h, v_h = workload_inputs(w)
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     out = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     mask = "causal" if w.causal else "none"
+    f32_tc = w.dtype == "f32" and w.D in (64, 128)
+    launches_per_step = 3 if f32_tc else 1  # fp32 on the tensor cores: two split kernels + main
+    ws = None
+    if f32_tc:
+        ws = torch.empty(int(lib.fa_mha_no_cache_f32_tc_workspace(w.B, w.S, w.Hkv, w.D)),
+                         dtype=torch.uint8, device=dev)
 
     def step():
-        fa.mha_no_cache(q, k, v, w.scale, mask, w.window, out=out, lse=lse)
+        fa.mha_no_cache(q, k, v, w.scale, mask, w.window, out=out, lse=lse, workspace=ws)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     if fa.device_status() != fa.FA_OK:
@@ -421,7 +431,7 @@ def bench_ours(args, w, world, rank, local, dist):
     clocks.start()
     t_wall = time.perf_counter()
     for s in range(args.steps):
-        flush.zero_()
+        flush()
         torch.cuda._sleep(SPIN_CYCLES)
         starts[s].record(stream)
         step()
@@ -432,40 +442,76 @@ def bench_ours(args, w, world, rank, local, dist):
     barrier(dist)
     kernel_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     local_ms = sum(kernel_ms)
+    mean_ms, median_ms = step_stats(kernel_ms)
     total_ms = max_over_ranks(local_ms, dist)
     if fa.device_status() != fa.FA_OK:
         raise RuntimeError("kernel reported a timed-out wait in the timed region")
 
-    # ---- end to end through the public API, host buffers, copies in the timed region
+    # ---- host cost of one call through the C ABI (argument checks, cached
+    # tensor maps, launch; no synchronisation), and of ctypes itself
+    dt = fa.DTYPE_BF16 if w.dtype == "bf16" else fa.DTYPE_F32
+    mcode = fa.MASK_CAUSAL if w.causal else fa.MASK_NONE
+    cargs = (out.data_ptr(), lse.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), w.B, w.S,
+             w.H, w.Hkv, w.D, w.scale, mcode, w.window)
+    if f32_tc:
+        def c_call():
+            lib.fa_mha_no_cache_f32_tc(*cargs, ws.data_ptr(), ws.numel(), stream.cuda_stream)
+    else:
+        def c_call():
+            lib.fa_mha_no_cache(*cargs, dt, stream.cuda_stream)
+    host_us = host_cost_us(c_call)
+    ctypes_us = host_cost_us(lambda: lib.fa_version())
+    py_us = host_cost_us(step)
+
+    # ---- end to end through the C ABI's host-buffer entry point: pinned host
+    # q, k, v in, pinned out and lse back, copies inside the timed region
     e2e = None
     if not args.no_e2e:
         qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
-        outps = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
-        bufs = [(q, k, v, out)] + [tuple(torch.empty_like(t) for t in (q, k, v, out))]
         e2e_steps = max(2, min(args.steps, 20))
+        st2 = [stream, torch.cuda.Stream(dev)]
+        ws_bytes = fa.host_workspace_bytes(w.B, w.S, w.H, w.Hkv, w.D, q_h.dtype)
+        wss = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in st2]
+        outps = [torch.empty(q_h.shape, dtype=q_h.dtype, pin_memory=True) for _ in st2]
+        lseps = [torch.empty((w.B, w.H, w.S), dtype=torch.float32, pin_memory=True)
+                 for _ in st2]
 
-        def copy_in(sl):
-            for d, h in zip(bufs[sl][:3], (qp, kp, vp)):
-                d.copy_(h, non_blocking=True)
+        def run_e2e(n):
+            # step i on stream i % 2 with its own workspace: step i+1's copy in
+            # overlaps step i's kernel, step i's copy out overlaps step i+1's
+            # kernel (separate copy engines for each direction)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            ev0.record(st2[0])
+            st2[1].wait_event(ev0)
+            done = [None, None]
+            for i in range(n):
+                sl = i % 2
+                if done[sl] is not None:
+                    st2[sl].wait_event(done[sl])
+                fa.mha_no_cache_host(qp, kp, vp, outps[sl], wss[sl], w.scale, mask, w.window,
+                                     lse=lseps[sl], stream=st2[sl])
+                done[sl] = torch.cuda.Event()
+                done[sl].record(st2[sl])
+            for sl in range(2):
+                if done[sl] is not None:
+                    st2[0].wait_event(done[sl])
+            ev1.record(st2[0])
+            torch.cuda.synchronize()
+            return ev0.elapsed_time(ev1) / n
 
-        def compute(sl):
-            qd, kd, vd, od = bufs[sl]
-            fa.mha_no_cache(qd, kd, vd, w.scale, mask, w.window, out=od)
-
-        def copy_out(sl):
-            outps[sl].copy_(bufs[sl][3], non_blocking=True)
-
-        pipelined_e2e_ms(2, copy_in, compute, copy_out, stream)  # warm-up
+        run_e2e(2)  # warm-up
         barrier(dist)
-        e2e_ms = max_over_ranks(
-            pipelined_e2e_ms(e2e_steps, copy_in, compute, copy_out, stream) * e2e_steps,
-            dist) / e2e_steps
+        e2e_ms = max_over_ranks(run_e2e(e2e_steps) * e2e_steps, dist) / e2e_steps
+        if fa.device_status() != fa.FA_OK:
+            raise RuntimeError("kernel reported a timed-out wait in the end-to-end run")
         h2d = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
-        d2h = outps[0].numel() * outps[0].element_size()
+        d2h = outps[0].numel() * outps[0].element_size() + lseps[0].numel() * 4
         e2e = {"value": world * workload_flops(w) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "pipeline": "two buffer sets: step i+1's copy in overlaps step i's kernel and "
-                           "copy out (three streams)"}
+               "api": "fa_mha_no_cache_host (C ABI, pinned host buffers)",
+               "pipeline": "steps alternate over two streams and workspaces: step i+1's copy "
+                           "in overlaps step i's kernel and copy out"}
 
     # ---- CPU baseline: the oracle on a bounded sample, rank 0 at N=1 only
     cpu = None
@@ -482,6 +528,14 @@ def bench_ours(args, w, world, rank, local, dist):
         cpu = {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
                "sample": f"{len(rows)} of {w.S} query rows (evenly spread), all {w.B} batches "
                          f"x {w.H} heads: {fl / 1e9:.1f} GFLOP in {t:.1f} s"}
+        if w.name in SINGLE_THREAD_WORKLOADS:
+            rows1 = oracle_sample_rows(w, rate / nthreads * args.cpu_seconds / 3)
+            t1 = run_oracle_sample(w, q_h, k_h, v_h, rows1, 1)
+            fl1 = sampled_flops(w, rows1)
+            cpu["single_thread"] = {
+                "value": fl1 / t1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                "sample": f"{len(rows1)} of {w.S} query rows: {fl1 / 1e9:.2f} GFLOP in "
+                          f"{t1:.1f} s"}
 
     flops = workload_flops(w)
     ms_per_step = total_ms / args.steps
@@ -494,29 +548,38 @@ def bench_ours(args, w, world, rank, local, dist):
         # useful fp32 FLOPs is the bf16 peak / 6.
         peak /= 6.0
         peak_note = "bf16 burst / 6 part products, MEASURED_PEAKS.json"
-    achieved = flops / (local_ms / args.steps * 1e-3) / 1e12
+    achieved = flops / (mean_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
+                "achieved_median": flops / (median_ms * 1e-3) / 1e12,
                 "traffic": prefill_traffic(w),
                 "peak_source": f"{peak_src} ({peak_note})"
                 if peak_src == "measured" else "fallback",
                 "algorithmic_bytes": algorithmic_bytes(w),
-                "hbm_gbs": algorithmic_bytes(w) / (local_ms / args.steps * 1e-3) / 1e9}
+                "hbm_gbs": algorithmic_bytes(w) / (mean_ms * 1e-3) / 1e9}
     return {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_per_step_median": median_ms,
+        "value_median": world * flops / (median_ms * 1e-3) / 1e12,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32 (three bf16 parts per value, fp32 accumulation)",
         "data": "synthetic",
         "config": {"workload": w.name, "shape": w.describe(), "B": w.B, "S": w.S, "H": w.H,
                    "Hkv": w.Hkv, "D": w.D, "mask": mask, "window": w.window,
-                   "flops_per_step": flops, "l2": "flushed (256 MiB write) before every step",
+                   "flops_per_step": flops, "l2": L2Flush.NOTE,
                    "timing": "CUDA events around each step; a GPU spin before the start event "
                              "hides host launch latency (e2e includes it)",
+                   "host_us_per_call": host_us,
+                   "host_us_note": "CPU time of one C-ABI call (checks, cached tensor maps, "
+                                   "launch; no sync) through ctypes, whose own cost is "
+                                   "ctypes_us_per_call; python_us_per_call is the Python "
+                                   "binding's call",
+                   "ctypes_us_per_call": ctypes_us, "python_us_per_call": py_us,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_peak": 100.0 * value / (peak * world),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "clocks": clocks.summary(), "gpu_launches": args.steps,
+        "clocks": clocks.summary(), "gpu_launches": args.steps * launches_per_step,
         "wall_s_timed_region": wall_s,
     }
 
@@ -575,7 +638,6 @@ def bench_kv_ours(args, w, world, rank, local, dist):
     q, k, v, lens = q_h.to(dev), k_h.to(dev), v_h.to(dev), lens_h.to(dev)
     out = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     mask = "causal" if w.causal else "none"
     splits, ws_bytes = fa.kv_cache_plan(w.B, w.Sq, w.S_cache, w.H, w.Hkv, w.D, mask, w.window,
@@ -590,14 +652,12 @@ def bench_kv_ours(args, w, world, rank, local, dist):
     # leave dirty lines whose write-back competes with the kernel's reads).
     cache_bytes = 2 * k.numel() * k.element_size()
     big_inputs = cache_bytes > 2 * L2_BYTES
-    if big_inputs:
-        flush = torch.empty(0, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev, enabled=not big_inputs)
     l2_note = (f"no flush: the step reads {cache_bytes / 1e6:.0f} MB of KV cache, more than "
-               f"the {L2_BYTES / 1e6:.0f} MB L2" if big_inputs
-               else "flushed (256 MiB write) before every step")
+               f"the {L2_BYTES / 1e6:.0f} MB L2" if big_inputs else L2Flush.NOTE)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     if fa.device_status() != fa.FA_OK:
@@ -609,7 +669,7 @@ def bench_kv_ours(args, w, world, rank, local, dist):
     torch.cuda.synchronize()
     clocks.start()
     for s in range(args.steps):
-        flush.zero_()
+        flush()
         torch.cuda._sleep(SPIN_CYCLES)
         starts[s].record(stream)
         step()
@@ -617,7 +677,9 @@ def bench_kv_ours(args, w, world, rank, local, dist):
     torch.cuda.synchronize()
     clocks.stop()
     barrier(dist)
-    local_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
+    kernel_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    local_ms = sum(kernel_ms)
+    _, median_ms = step_stats(kernel_ms)
     total_ms = max_over_ranks(local_ms, dist)
     if fa.device_status() != fa.FA_OK:
         raise RuntimeError("kernel reported a timed-out wait in the timed region")
@@ -673,6 +735,7 @@ def bench_kv_ours(args, w, world, rank, local, dist):
     return {
         "metric": KV_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_per_step_median": median_ms, "value_median": world * byts / (median_ms * 1e-3) / 1e9,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "shape": w.describe(), "B": w.B, "Sq": w.Sq,
@@ -749,14 +812,14 @@ def bench_topk_ours(args, w, world, rank, local, dist):
     # launch reading all of them from DRAM; a flush would instead leave L2
     # full of dirty lines that the kernel pays to write back.
     big = scores.numel() * 4 > L2_BYTES
-    flush = torch.empty(0 if big else L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev, enabled=not big)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         fa.topk(scores, w.K, values=values, indices=indices, workspace=ws)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -766,7 +829,7 @@ def bench_topk_ours(args, w, world, rank, local, dist):
     torch.cuda.synchronize()
     clocks.start()
     for s in range(args.steps):
-        flush.zero_()
+        flush()
         torch.cuda._sleep(SPIN_CYCLES)
         starts[s].record(stream)
         step()
@@ -774,7 +837,9 @@ def bench_topk_ours(args, w, world, rank, local, dist):
     torch.cuda.synchronize()
     clocks.stop()
     barrier(dist)
-    local_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
+    kernel_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    local_ms = sum(kernel_ms)
+    _, median_ms = step_stats(kernel_ms)
     total_ms = max_over_ranks(local_ms, dist)
     byts = topk_bytes(w)
     ms_per_step = total_ms / args.steps
@@ -823,13 +888,14 @@ def bench_topk_ours(args, w, world, rank, local, dist):
     return {
         "metric": TOPK_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "ms_per_step_median": median_ms, "value_median": world * byts / (median_ms * 1e-3) / 1e9,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": w.name, "shape": w.describe(), "B": w.B, "V": w.V, "K": w.K,
                    "chunks_per_row": chunks, "bytes_per_step": byts,
                    "l2": (f"no flush: the step reads {scores.numel() * 4 / 1e6:.0f} MB, more "
                           f"than the {L2_BYTES / 1e6:.0f} MB L2") if big
-                   else "flushed (256 MiB write) before every step",
+                   else L2Flush.NOTE,
                    "timing": "CUDA events around each step; a GPU spin before the start event "
                              "hides host launch latency (e2e includes it)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

@@ -44,7 +44,8 @@ typedef enum {
   FA_ERR_INVALID_ARG = 1, /* a null pointer, a bad size, a bad mask/window */
   FA_ERR_UNSUPPORTED = 2, /* valid but not built: D, dtype, GPU arch, alignment */
   FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
-  FA_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait (see fa_device_status) */
+  FA_ERR_TIMEOUT = 4,     /* a kernel gave up on a bounded wait (see fa_stream_status) */
+  FA_ERR_BOUNDS = 5       /* debug build only: a bounds guard skipped an out-of-range access */
 } fa_status_t;
 
 /*
@@ -77,10 +78,16 @@ typedef enum {
  * Behaviour: asynchronous on `stream`; returns after validation and launch.
  * Argument errors return FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED before any
  * CUDA call. A kernel that exceeds its bounded-wait limit abandons its tile,
- * sets a sticky per-device status word and leaves the outputs of that tile
- * undefined; read it with fa_device_status(). The first call on a device
- * allocates that 4-byte status word (cudaMalloc) and sets kernel attributes;
- * fa_shutdown() frees it. Thread-safe.
+ * sets the sticky status word of `stream` and leaves the outputs of that
+ * tile undefined; read it with fa_stream_status(stream) (ordered on that
+ * stream only) or fa_device_status() (every stream of a device).
+ *
+ * Per-device state, created lazily and freed by fa_shutdown(): the first
+ * call on a device allocates that device's status words (one 4 KB cudaMalloc)
+ * and raises each kernel's shared-memory limit once; the TMA tensor maps of
+ * a call are cached, keyed on address, sizes and strides, so a repeated call
+ * on the same buffers encodes nothing. Make the first call on a device before
+ * any stream capture. Thread-safe.
  */
 fa_status_t fa_mha_no_cache(void *out, float *lse, const void *q, const void *k, const void *v,
                             int B, int S, int H, int Hkv, int D, float scale, int mask_kind,
@@ -119,14 +126,18 @@ fa_status_t fa_mha_no_cache_strided(void *out, float *lse, const void *q, const 
  * 4-byte status word) lives in a 256-byte array inside this library that
  * every GPU loading the library holds until the process exits; sizes that
  * would need more scratch than that are rejected with FA_ERR_UNSUPPORTED
- * (the status word does not grow with B, S, H or D, so every size accepted
- * by fa_mha_no_cache fits).
+ * (the status word does not grow with B, S, H or D, so no size is).
  *
  * Arguments are those of fa_mha_no_cache for dtype FA_DTYPE_BF16 (the only
- * dtype it takes), plus check_status: when non-zero the call synchronises
- * `stream` after the launch and returns FA_ERR_TIMEOUT if the kernel gave up
- * on a bounded wait (default 2 s limit); when zero it returns right after the
- * launch. Each call clears the status word on `stream` before its launch.
+ * dtype it takes) with D a multiple of 8 up to 128 (the head dims of the
+ * prefill kernel; larger ones are rejected with FA_ERR_UNSUPPORTED), plus
+ * check_status: when non-zero the call synchronises `stream` after the
+ * launch and returns FA_ERR_TIMEOUT if the kernel gave up on a bounded wait
+ * (the limit set by fa_set_wait_timeout_ns); when zero it returns right after
+ * the launch, and a time-out is then reported nowhere: the outputs of the
+ * abandoned tiles are undefined and the next call clears the word. Each call
+ * clears the status word on `stream` before its launch. The word is not one
+ * of the words fa_stream_status and fa_device_status read.
  *
  * The first call on each device resolves the array's device address (a
  * cudaGetSymbolAddress set-up step); make that first call before any stream
@@ -138,6 +149,35 @@ fa_status_t fa_mha_no_cache_noalloc(void *out, float *lse, const void *q, const 
                                     const void *v, int B, int S, int H, int Hkv, int D,
                                     float scale, int mask_kind, int local_window_size,
                                     void *stream, int check_status);
+
+/*
+ * fa_mha_no_cache_host -- fa_mha_no_cache with q, k, v, out and lse in HOST
+ * memory: enqueues on `stream` the copies of q, k and v into `workspace`, the
+ * forward, and the copies of out (and lse) back to the host. Returns after
+ * enqueueing; the host outputs are complete once `stream` has been
+ * synchronised. With page-locked (pinned) host buffers every copy is
+ * asynchronous, so calls alternating over two streams (each with its own
+ * workspace) overlap one call's copies with the other's kernel; with
+ * pageable buffers CUDA performs the copies synchronously.
+ *
+ *   out, lse, q, k, v : host, layouts as fa_mha_no_cache (dense); lse may be
+ *             NULL.
+ *   workspace, workspace_bytes : caller-owned device buffer of at least
+ *             fa_mha_no_cache_host_workspace(B, S, H, Hkv, D, dtype) bytes,
+ *             256-byte aligned; it receives the device copies of q, k, v,
+ *             out and lse (and, for fp32 with D 64 or 128, the bf16 parts of
+ *             K and V: that case runs on the tensor cores as
+ *             fa_mha_no_cache_f32_tc).
+ * Every other argument, and the error behaviour, as fa_mha_no_cache; all
+ * arguments are checked before the first copy is enqueued.
+ */
+fa_status_t fa_mha_no_cache_host(void *out, float *lse, const void *q, const void *k,
+                                 const void *v, int B, int S, int H, int Hkv, int D, float scale,
+                                 int mask_kind, int local_window_size, int dtype, void *workspace,
+                                 unsigned long long workspace_bytes, void *stream);
+
+/* Device bytes fa_mha_no_cache_host needs (0 for sizes below 1 or a bad dtype). */
+unsigned long long fa_mha_no_cache_host_workspace(int B, int S, int H, int Hkv, int D, int dtype);
 
 /*
  * fa_mha_no_cache_f32_tc -- fa_mha_no_cache for fp32 tensors on the tensor
@@ -246,10 +286,26 @@ fa_status_t fa_topk_plan(int B, int V, int K, int num_sms, int *chunks_out,
                          unsigned long long *workspace_bytes_out);
 
 /*
+ * fa_stream_status -- the sticky status of the work this library enqueued on
+ * `stream` (a cudaStream_t of the current device, as void*; NULL = legacy
+ * default stream): FA_OK, FA_ERR_TIMEOUT if a kernel launched on that stream
+ * since the last clear abandoned a bounded wait, or FA_ERR_BOUNDS (debug
+ * build) if a bounds guard fired. The read is a copy ordered on `stream`
+ * followed by cudaStreamSynchronize(stream): it waits for that stream's work
+ * only, never for the device. With clear != 0 the word is reset (also on
+ * `stream`). Each stream has its own word for the first 1023 streams used on
+ * a device; later streams share one word. A stream handle that is destroyed
+ * and re-created at the same address keeps the old stream's word until it is
+ * cleared. Returns FA_ERR_CUDA if the copy or the synchronisation fails.
+ */
+fa_status_t fa_stream_status(void *stream, int clear);
+
+/*
  * fa_device_status -- synchronises `device` (cudaDeviceSynchronize) and reads
- * its sticky status word: FA_OK, or FA_ERR_TIMEOUT if any kernel since the
- * last clear abandoned a bounded wait. With clear != 0 the word is reset.
- * Returns FA_ERR_CUDA if the synchronisation itself reports an error.
+ * the status words of all its streams: FA_OK, FA_ERR_TIMEOUT if any kernel
+ * since the last clear abandoned a bounded wait, FA_ERR_BOUNDS (debug build)
+ * if a bounds guard fired. With clear != 0 every word is reset. Returns
+ * FA_ERR_CUDA if the synchronisation itself reports an error.
  */
 fa_status_t fa_device_status(int device, int clear);
 
@@ -272,7 +328,7 @@ unsigned long long fa_set_wait_timeout_ns(unsigned long long ns);
 int fa_set_stall_probe(int enable);
 
 /* fa_status_string -- a static, human-readable name for a status code. */
-const char *fa_status_string(int status);
+const char *fa_status_string(fa_status_t status);
 
 /*
  * fa_last_error_message -- detail of the last non-OK status returned on the
@@ -285,8 +341,44 @@ const char *fa_last_error_message(void);
 int fa_version(void);
 
 /*
- * fa_shutdown -- frees the per-device status words. Call only when no work
- * issued by this library is pending; later calls re-create what they need.
+ * fa_trace_set_buffer -- debug build (libfa_mha_debug.so, compiled with
+ * FA_TRACE=1) only: record an event trace of every later launch of the
+ * bf16 prefill kernel (D <= 128) into `buf`, a caller-owned, 16-byte-aligned
+ * device buffer of `bytes` bytes: fa_trace_bytes_per_cta() bytes for each
+ * CTA, CTA c at offset c * fa_trace_bytes_per_cta(); CTAs past the buffer
+ * record nothing. Each CTA holds 4 roles (TMA producer, MMA issuer, softmax
+ * of Q tile 0, softmax of Q tile 1) x 128 records of 16 bytes: global timer
+ * in ns (two 32-bit words), the SM's clock (low 32 bits), and event code <<
+ * 24 | 24-bit argument; the codes are listed in csrc/fa_trace.cuh. A role's
+ * records past 128 are dropped; records not written are left as they were
+ * (zero the buffer first). NULL stops tracing. The default build returns
+ * FA_ERR_UNSUPPORTED (and FA_OK for NULL).
+ */
+fa_status_t fa_trace_set_buffer(void *buf, unsigned long long bytes);
+
+/* fa_trace_bytes_per_cta -- trace bytes per CTA (0 in the default build). */
+unsigned long long fa_trace_bytes_per_cta(void);
+
+/*
+ * fa_trace_ctas -- CTAs of one bf16 prefill launch (D <= 128) for these
+ * sizes: one per (256-query block, head, batch); 0 for sizes that launch
+ * another kernel.
+ */
+long long fa_trace_ctas(int B, int S, int H, int D);
+
+/*
+ * fa_debug_set_lse_limit -- debug build only: the number of LSE elements the
+ * prefill kernel's bounds guard lets it write (0: all B * H * S). Elements
+ * past the limit are skipped and the stream's status reports FA_ERR_BOUNDS.
+ * Exists to test that the guards fire; the default build returns
+ * FA_ERR_UNSUPPORTED.
+ */
+fa_status_t fa_debug_set_lse_limit(long long elems);
+
+/*
+ * fa_shutdown -- frees the per-device status words and empties the tensor-map
+ * cache. Call only when no work issued by this library is pending; later
+ * calls re-create what they need.
  */
 void fa_shutdown(void);
 

@@ -138,3 +138,76 @@ def test_f32_tensor_core_workspace_size(lib):
     plane = 2 * 100 * 4 * 128 * 2
     assert lib.fa_mha_no_cache_f32_tc_workspace(2, 100, 4, 128) == 6 * (-(-plane // 256) * 256)
     assert lib.fa_mha_no_cache_f32_tc_workspace(2, 100, 4, 96) == 0
+
+
+def test_status_string_names_the_bounds_status(lib):
+    assert lib.fa_status_string(fa.FA_ERR_BOUNDS) == b"FA_ERR_BOUNDS"
+
+
+def test_trace_and_guard_knobs_are_debug_only(lib):
+    # The default build has no trace and no guards; turning tracing off is
+    # always accepted. None of these calls touches CUDA.
+    assert lib.fa_trace_bytes_per_cta() == 0
+    assert lib.fa_trace_set_buffer(None, 0) == fa.FA_OK
+    assert lib.fa_trace_set_buffer(P, 1 << 20) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_debug_set_lse_limit(10) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_trace_cta_count_follows_the_prefill_grid(lib):
+    # one CTA per (256-query block, head, batch); head dims above 128 run
+    # another kernel and have no trace
+    assert lib.fa_trace_ctas(4, 1024, 16, 64) == 4 * 16 * 4
+    assert lib.fa_trace_ctas(2, 4097, 32, 128) == 17 * 32 * 2
+    assert lib.fa_trace_ctas(1, 1, 1, 8) == 1
+    assert lib.fa_trace_ctas(1, 100, 2, 256) == 0
+    assert lib.fa_trace_ctas(0, 100, 2, 64) == 0
+
+
+def test_debug_build_exports_the_same_symbols_and_traces():
+    dbg = fa.load_debug_library()
+    for name in _declared_functions():
+        assert hasattr(dbg, name), name
+    assert dbg.fa_trace_bytes_per_cta() == 4 * 128 * 16
+    assert dbg.fa_trace_set_buffer(P + 8, 1 << 20) == fa.FA_ERR_INVALID_ARG  # 16-byte aligned
+    assert dbg.fa_debug_set_lse_limit(-1) == fa.FA_ERR_INVALID_ARG
+    assert dbg.fa_debug_set_lse_limit(0) == fa.FA_OK
+    assert dbg.fa_trace_set_buffer(None, 0) == fa.FA_OK
+
+
+def _call_host(lib, out=P, q=P, k=P, v=P, B=1, S=8, H=2, Hkv=2, D=64, ws=P, ws_bytes=1 << 30,
+               dtype=0, window=-1):
+    return lib.fa_mha_no_cache_host(out, None, q, k, v, B, S, H, Hkv, D, 0.125, 1, window, dtype,
+                                    ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=None), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=P + 16), fa.FA_ERR_INVALID_ARG),       # 256-byte aligned workspace
+    (dict(ws_bytes=1024), fa.FA_ERR_INVALID_ARG),   # too small
+    (dict(H=3, Hkv=2), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(window=0), fa.FA_ERR_INVALID_ARG),
+    (dict(D=100), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=5), fa.FA_ERR_UNSUPPORTED),
+])
+def test_host_entry_point_checks_everything_before_copying(lib, kw, code):
+    assert _call_host(lib, **kw) == code
+    assert lib.fa_last_error_message()
+
+
+def test_host_entry_point_workspace_size(lib):
+    def a(x):
+        return -(-x // 256) * 256
+    B, S, H, Hkv, D = 2, 100, 4, 2, 64
+    q, kv, lse = B * S * H * D * 2, B * S * Hkv * D * 2, B * H * S * 4
+    assert lib.fa_mha_no_cache_host_workspace(B, S, H, Hkv, D, 0) == \
+        a(a(a(a(q) + kv) + kv) + q) + a(lse)
+    # fp32 at D 64 / 128 also holds the six bf16 planes of K and V
+    q4, kv4 = 2 * q, 2 * kv
+    base = a(a(a(a(q4) + kv4) + kv4) + q4) + a(lse)
+    assert lib.fa_mha_no_cache_host_workspace(B, S, H, Hkv, D, 1) == \
+        base + lib.fa_mha_no_cache_f32_tc_workspace(B, S, Hkv, D)
+    assert lib.fa_mha_no_cache_host_workspace(B, S, H, Hkv, 32, 1) == \
+        a(a(a(a(q4 // 2) + kv4 // 2) + kv4 // 2) + q4 // 2) + a(lse)
+    assert lib.fa_mha_no_cache_host_workspace(0, S, H, Hkv, D, 0) == 0
