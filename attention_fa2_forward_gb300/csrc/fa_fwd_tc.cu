@@ -121,9 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   namespace tr = trace;
   const int trace_role = warp == kLoadWarp ? tr::kRoleProducer
                          : warp == kMmaWarp ? tr::kRoleMma
-                                            : tr::kRoleSoftmax0 + (warp >> 2);
-  tr::Recorder rec(p.trace, p.trace_ctas, trace_role,
-                   lane == 0 && (warp >= kSoftmaxWarps || (warp & 3) == 0));
+                                            : tr::softmax_role(warp);
+  tr::Recorder rec(p.trace, p.trace_ctas, trace_role, lane == 0);
   if (warp == kLoadWarp) rec(tr::kCtaStart, tr::sm_id());
 
   // ---- work item: heaviest (last) query blocks first
@@ -296,13 +295,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         rec(tr::kPvIssued, (t << 16) | j);
       };
       uint32_t p_phase[kQTiles] = {0u, 0u};
-      auto wait_p = [&](int t) -> bool {
+      auto wait_p = [&](int t, int j) -> bool {
         if (aborted() || !ptx::mbar_wait(bar_p_full + 8 * t, p_phase[t], limit)) {
           fail();
           return false;
         }
         p_phase[t] ^= 1u;
         ptx::tc_fence_after();
+        rec(tr::kPSeen, (t << 16) | j);
         return true;
       };
 
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vs = wait_kv(2 * rel + 1);
         if (vs < 0) break;
         if (in_tile(0, j)) {
-          if (!wait_p(0)) break;
+          if (!wait_p(0, j)) break;
           issue_pv(0, vs, j > lo[0], j);
           if (j == hi[0] - 1) ptx::tc_commit(bar_o_full);
         }
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (in_tile(0, j + 1)) issue_s(0, ks, j + 1);
         }
         if (in_tile(1, j)) {
-          if (!wait_p(1)) break;
+          if (!wait_p(1, j)) break;
           issue_pv(1, vs, j > lo[1], j);
           if (j == hi[1] - 1) ptx::tc_commit(bar_o_full + 8);
         }
@@ -391,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = 0; c0 < kBN; c0 += 32) ptx::tmem_ld_32x32b_x32(tS + c0, r + c0);
       ptx::tmem_wait_ld();
       ptx::reg_fence<kBN>(r);
+      rec(tr::kSLoaded, j);
 
       const int k0 = j * kBN;
       bool full = k0 + kBN <= p.S;
@@ -406,6 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // Row maximum of the (visible) scores.
       const float mx = tile::row_max(r);
+      if (FA_TRACE) {
+        asm volatile("" ::"f"(mx));
+        rec(tr::kMaxDone, j);
+      }
       const float m_tile = mx == -INFINITY ? -INFINITY : mx * ce;
       const float m_new = fmaxf(m_use, m_tile);
       const bool first = j == tlo;
@@ -424,6 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // written over S, and the row sum.
       const float row_sum = tile::exp2_to_bf16(r, ce, neg_base);
       l_run = l_run * alpha + row_sum;
+      if (FA_TRACE) {
+        asm volatile("" ::"f"(l_run), "r"(r[0]), "r"(r[63]));
+        rec(tr::kExpDone, j);
+      }
 #pragma unroll
       for (int c0 = 0; c0 < kBN / 2; c0 += 32) ptx::tmem_st_32x32b_x32(tS + c0, r + c0);
 

@@ -1,7 +1,8 @@
-// fa_tile.cuh -- per-row arithmetic on one 128-key score tile, shared by the
-// tensor-core kernels (prefill and KV-cache). A softmax thread owns one query
-// row (one tensor-memory lane) and holds that row's 128 fp32 scores as bit
-// patterns in registers.
+// fa_tile.cuh -- per-row arithmetic on the score columns of one 128-key tile,
+// shared by the tensor-core kernels (prefill and KV-cache). A softmax thread
+// owns N columns of one query row (one tensor-memory lane): all 128 in the
+// KV-cache kernel, one half in the prefill kernel, where two threads share a
+// row. It holds them as fp32 bit patterns in registers.
 #pragma once
 
 #include <cstdint>
@@ -14,29 +15,33 @@ namespace tile {
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr uint32_t kNegInfBits = 0xff800000u;
 
-// Hides (-inf) the scores outside the visible key columns [vlo, vhi] of the
-// tile; with a zero scale the visible ones become 0 (the caller then uses 1
-// as the multiplier, which keeps -inf * 0 out of the hidden lanes).
-// Branch-free: one unsigned range test and two selects per element.
+// Hides (-inf) the scores outside the visible columns [vlo, vhi] (relative
+// to the first of the N held columns); with a zero scale the visible ones
+// become 0 (the caller then uses 1 as the multiplier, which keeps -inf * 0
+// out of the hidden lanes). Branch-free: one unsigned range test and two
+// selects per element.
+template <int N = kBN>
 __device__ __forceinline__ void mask_cols(uint32_t* r, int vlo, int vhi, bool zero_scale) {
   int lo = max(vlo, 0);
-  const int hi = min(vhi, kBN - 1);
+  const int hi = min(vhi, N - 1);
   unsigned span = static_cast<unsigned>(hi - lo);
-  if (hi < lo) {  // nothing visible in this tile
-    lo = 2 * kBN;
+  if (hi < lo) {  // nothing visible in these columns
+    lo = 2 * N;
     span = 0;
   }
   const uint32_t keep = zero_scale ? 0u : 0xffffffffu;
 #pragma unroll
-  for (int e = 0; e < kBN; ++e)
+  for (int e = 0; e < N; ++e)
     r[e] = static_cast<unsigned>(e - lo) <= span ? (r[e] & keep) : kNegInfBits;
 }
 
-// Maximum of the row's scores (four independent max3 chains).
+// Maximum of the N held scores (four independent max3 chains).
+template <int N = kBN>
 __device__ __forceinline__ float row_max(const uint32_t* r) {
+  static_assert(N % 8 == 0, "columns");
   float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < kBN; e += 8) {
+  for (int e = 0; e < N; e += 8) {
     a0 = ptx::max3(a0, __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
     a1 = ptx::max3(a1, __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
     a2 = ptx::max3(a2, __uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
@@ -45,15 +50,16 @@ __device__ __forceinline__ float row_max(const uint32_t* r) {
   return ptx::max3(a0, a1, fmaxf(a2, a3));
 }
 
-// P = 2^(s * ce + neg_base) for the row's 128 scores (hidden scores are -inf
-// and give 0), written as 64 bf16 pairs over r[0..63]; returns the fp32 sum
-// of the (unrounded) P. Pairs of columns use packed FMAs and adds.
+// P = 2^(s * ce + neg_base) for the N held scores (hidden scores are -inf
+// and give 0), written as N/2 bf16 pairs over r[0..N/2-1]; returns the fp32
+// sum of the (unrounded) P. Pairs of columns use packed FMAs and adds.
+template <int N = kBN>
 __device__ __forceinline__ float exp2_to_bf16(uint32_t* r, float ce, float neg_base) {
   const uint64_t c2 = ptx::pair(__float_as_uint(ce), __float_as_uint(ce));
   const uint64_t nb2 = ptx::pair(__float_as_uint(neg_base), __float_as_uint(neg_base));
   uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
 #pragma unroll
-  for (int i = 0; i < kBN / 2; ++i) {
+  for (int i = 0; i < N / 2; ++i) {
     uint32_t lo, hi;
     ptx::unpair(ptx::fma2(ptx::pair(r[2 * i], r[2 * i + 1]), c2, nb2), lo, hi);
     lo = __float_as_uint(ptx::ex2_approx(__uint_as_float(lo)));

@@ -2,9 +2,9 @@
 // build (FA_TRACE=1, library libfa_mha_debug.so).
 //
 // Trace: each CTA of the prefill kernel owns kRoles x kEventsPerRole records
-// of 16 bytes in a caller-provided device buffer; one thread of each warp
-// role (TMA producer, MMA issuer, the softmax warpgroup of each Q tile)
-// appends its events in program order:
+// of 16 bytes in a caller-provided device buffer; lane 0 of each warp (TMA
+// producer, MMA issuer, the eight softmax warps) appends its events in
+// program order:
 //   x, y : %globaltimer (ns), low and high word -- comparable across SMs;
 //   z    : low word of %clock64 of the SM -- cycle-accurate within a CTA;
 //   w    : event code << 24 | 24-bit argument.
@@ -34,13 +34,20 @@
 namespace fa {
 namespace trace {
 
-constexpr int kRoles = 4;            // producer, MMA issuer, softmax tile 0, softmax tile 1
+// producer, MMA issuer, softmax warp 0 (tile 0) and 4 (tile 1), then softmax
+// warps 1, 2, 3, 5, 6, 7
+constexpr int kRoles = 10;
 constexpr int kEventsPerRole = 128;
 constexpr int kRecordBytes = 16;
 constexpr unsigned long long kBytesPerCta =
     static_cast<unsigned long long>(kRoles) * kEventsPerRole * kRecordBytes;
 
 enum Role : int { kRoleProducer = 0, kRoleMma = 1, kRoleSoftmax0 = 2, kRoleSoftmax1 = 3 };
+
+// Role of softmax warp w (0-7) of the prefill kernel.
+__host__ __device__ constexpr int softmax_role(int w) {
+  return w == 0 ? kRoleSoftmax0 : w == 4 ? kRoleSoftmax1 : (w < 4 ? 3 + w : 2 + w);
+}
 
 // Event codes (the argument's meaning in brackets).
 enum Code : uint32_t {
@@ -56,6 +63,10 @@ enum Code : uint32_t {
   kPReady = 10,       // softmax: P(j) stored, O corrected [KV tile j | rescaled << 23]
   kEpilogueStart = 11,  // softmax: O(final) is ready [0]
   kEpilogueEnd = 12,    // softmax: O stored, LSE written [0]
+  kSLoaded = 13,        // softmax: S(j) is in registers [KV tile j]
+  kMaxDone = 14,        // softmax: row maximum known [KV tile j]
+  kExpDone = 15,        // softmax: P(j) computed, not yet stored [KV tile j]
+  kPSeen = 16,          // MMA issuer: all of P(j) is in tensor memory [Q tile << 16 | j]
 };
 
 // Appends events of one role of one CTA. Construct in the thread that

@@ -13,10 +13,14 @@ import torch
 
 from . import _mask_code, load_debug_library
 
-ROLES = ("producer", "mma", "softmax0", "softmax1")
+# "softmax0" / "softmax1": warp 0 / 4, the first warp of Q tile 0 / 1; the
+# other softmax warps follow ("softmax0_w1" = warp 1, ...).
+ROLES = ("producer", "mma", "softmax0", "softmax1", "softmax0_w1", "softmax0_w2",
+         "softmax0_w3", "softmax1_w1", "softmax1_w2", "softmax1_w3")
 CODES = {1: "cta_start", 2: "q_load_issued", 3: "k_load_issued", 4: "v_load_issued",
          5: "q_ready", 6: "s_issued", 7: "pv_issued", 8: "mma_drained", 9: "s_ready",
-         10: "p_ready", 11: "epilogue_start", 12: "epilogue_end"}
+         10: "p_ready", 11: "epilogue_start", 12: "epilogue_end", 13: "s_loaded",
+         14: "max_done", 15: "exp_done", 16: "p_seen"}
 EVENTS_PER_ROLE = 128
 
 

@@ -346,8 +346,9 @@ int fa_version(void);
  * bf16 prefill kernel (D <= 128) into `buf`, a caller-owned, 16-byte-aligned
  * device buffer of `bytes` bytes: fa_trace_bytes_per_cta() bytes for each
  * CTA, CTA c at offset c * fa_trace_bytes_per_cta(); CTAs past the buffer
- * record nothing. Each CTA holds 4 roles (TMA producer, MMA issuer, softmax
- * of Q tile 0, softmax of Q tile 1) x 128 records of 16 bytes: global timer
+ * record nothing. Each CTA holds 10 roles (TMA producer, MMA issuer, softmax
+ * warps 0 and 4 -- the first of Q tile 0 and of Q tile 1 -- then softmax
+ * warps 1, 2, 3, 5, 6, 7) x 128 records of 16 bytes: global timer
  * in ns (two 32-bit words), the SM's clock (low 32 bits), and event code <<
  * 24 | 24-bit argument; the codes are listed in csrc/fa_trace.cuh. A role's
  * records past 128 are dropped; records not written are left as they were
