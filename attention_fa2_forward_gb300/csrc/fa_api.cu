@@ -156,7 +156,7 @@ struct MapKey {
   const void* base;
   long long dims[4];
   long long strides[3];
-  int box_heads, box_rows;
+  int box_heads, box_rows, box_cols, pad;
   bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(*this)) == 0; }
 };
 struct MapKeyHash {
@@ -168,7 +168,7 @@ struct MapKeyHash {
     return static_cast<size_t>(h);
   }
 };
-static_assert(sizeof(MapKey) == 8 + 4 * 8 + 3 * 8 + 2 * 4, "MapKey must have no padding");
+static_assert(sizeof(MapKey) == 8 + 4 * 8 + 3 * 8 + 4 * 4, "MapKey must have no padding");
 constexpr size_t kMapCacheMax = 4096;  // entries; the cache is emptied when it would grow past
 std::mutex g_map_mutex;
 std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
@@ -194,7 +194,9 @@ cudaError_t ensure_smem_attr(unsigned long long* done, const void* func, int byt
 }
 
 bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D,
-                            BshdStrides st, int box_heads, int box_rows, bool use_cache) {
+                            BshdStrides st, int box_heads, int box_rows, bool use_cache,
+                            int box_cols) {
+  if (box_cols != 64 && box_cols != 32) return false;
   st = resolve_strides(st, S, heads, D);
   MapKey key;
   std::memset(&key, 0, sizeof(key));
@@ -208,6 +210,7 @@ bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, in
   key.strides[2] = st.b;
   key.box_heads = box_heads;
   key.box_rows = box_rows;
+  key.box_cols = box_cols;
   if (use_cache) {
     std::lock_guard<std::mutex> lock(g_map_mutex);
     auto it = g_map_cache.find(key);
@@ -224,12 +227,14 @@ bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, in
                                  static_cast<cuuint64_t>(st.s) * 2,
                                  static_cast<cuuint64_t>(st.b) * 2};
   if (box_heads < 1 || box_heads > 256 || box_rows < 1 || box_rows > 256) return false;
-  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_heads),
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols),
+                             static_cast<cuuint32_t>(box_heads),
                              static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   if (!use_cache) return true;

@@ -142,13 +142,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: heaviest (last) query blocks first.
-  const int per_qb = p.H * p.B;
-  const int qb = num_qblocks - 1 - static_cast<int>(blockIdx.x / per_qb);
-  const int rem = static_cast<int>(blockIdx.x % per_qb);
-  const int h = rem % p.H;
-  const int b = rem / p.H;
-  const int hk = h / (p.H / p.Hkv);
+  // Work item: the CTAs of one (batch, KV head) -- every query block of each
+  // of its G query heads -- are consecutive, heaviest (last) query blocks
+  // first, so the K/V planes they all stream stay in L2 while they run
+  // (query block major, the planes were read from DRAM again by each wave).
+  const int G = p.H / p.Hkv;
+  const int per_group = num_qblocks * G;
+  const int grp = static_cast<int>(blockIdx.x / per_group);
+  const int rem = static_cast<int>(blockIdx.x % per_group);
+  const int qb = num_qblocks - 1 - rem / G;
+  const int hk = grp % p.Hkv;
+  const int b = grp / p.Hkv;
+  const int h = hk * G + rem % G;
   const int q0 = qb * kBM;
   const int kv_end = p.causal ? min(p.S, q0 + kBM)
                               : (p.window > 0 ? min(p.S, q0 + kBM - 1 + p.window) : p.S);

@@ -56,16 +56,24 @@ constexpr int kSoftmaxWarps = 4 * kQTiles;        // one warpgroup per Q tile
 constexpr int kMmaWarp = kSoftmaxWarps;           // warp 8
 constexpr int kLoadWarp = kSoftmaxWarps + 1;      // warp 9
 constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
-constexpr int kBoxBytes = kBN * 128;              // [128 rows][64 bf16], 128B-swizzled
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr unsigned long long kDrainExtraNs = 100000000ull;  // 100 ms
 
+// Tiles of 128 rows x D bf16 columns are held as TMA boxes of [128][64] with
+// the 128-byte swizzle (D = 64, 128) or, for D = 96, of [128][32] with the
+// 64-byte swizzle (three boxes: the MMAs then run with K = 96 and N = 96, no
+// padding columns).
 template <int D>
 struct Cfg {
-  static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kBoxes = D / 64;
+  static_assert(D == 64 || D == 96 || D == 128, "head dim");
+  static constexpr int kBoxCols = D == 96 ? 32 : 64;
+  static constexpr int kRowBytes = kBoxCols * 2;          // bytes of one box row (= swizzle span)
+  static constexpr int kBoxBytes = kBM * kRowBytes;
+  static constexpr int kBoxes = D / kBoxCols;
+  static constexpr int kKPerBox = kBoxCols / 16;          // MMA K steps of 16 per box
+  static constexpr uint32_t kSwizzle = D == 96 ? ptx::kSwizzle64B : ptx::kSwizzle128B;
   static constexpr int kTileBytes = kBoxes * kBoxBytes;  // one [128][D] bf16 tile
   static constexpr int kStages = D == 128 ? 4 : 6;       // K/V ring slots
   static constexpr int kQOff = 0;
@@ -202,8 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive_expect_tx(bar_q_full + 8 * t, C::kTileBytes);
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx)
-            ptx::tma_load_4d(sQ + t * C::kTileBytes + bx * kBoxBytes, &tm_q, bar_q_full + 8 * t,
-                             bx * 64, h, q0[t], b, pol_q);
+            ptx::tma_load_4d(sQ + t * C::kTileBytes + bx * C::kBoxBytes, &tm_q, bar_q_full + 8 * t,
+                             bx * C::kBoxCols, h, q0[t], b, pol_q);
           rec(tr::kQLoadIssued, t);
         }
       }
@@ -226,8 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const CUtensorMap* tm = kind == 0 ? &tm_k : &tm_v;
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx)
-            ptx::tma_load_4d(sKV + s * C::kTileBytes + bx * kBoxBytes, tm, bar_kv_full + 8 * s,
-                             bx * 64, hk, j * kBN, b, pol_kv);
+            ptx::tma_load_4d(sKV + s * C::kTileBytes + bx * C::kBoxBytes, tm, bar_kv_full + 8 * s,
+                             bx * C::kBoxCols, hk, j * kBN, b, pol_kv);
           rec(kind == 0 ? tr::kKLoadIssued : tr::kVLoadIssued, j);
           armed |= 1u << s;
           armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
@@ -271,15 +279,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         return s;
       };
-      const uint64_t dq0 = ptx::smem_desc_sw128(sQ, 16, 1024);
-      const uint64_t dk0 = ptx::smem_desc_sw128(sKV, 16, 1024);
-      const uint64_t dv0 = ptx::smem_desc_sw128(sKV, kBoxBytes, 1024);
+      // K-major Q and K: 8-row groups 8 box rows apart. MN-major V: atoms
+      // of kBoxCols columns one box apart.
+      const uint64_t dq0 = ptx::smem_desc(sQ, 16, 8 * C::kRowBytes, C::kSwizzle);
+      const uint64_t dk0 = ptx::smem_desc(sKV, 16, 8 * C::kRowBytes, C::kSwizzle);
+      const uint64_t dv0 = ptx::smem_desc(sKV, C::kBoxBytes, 8 * C::kRowBytes, C::kSwizzle);
       auto issue_s = [&](int t, int kslot, int j) {
         const uint64_t dq = dq0 + static_cast<uint32_t>((t * C::kTileBytes) >> 4);
         const uint64_t dk = dk0 + static_cast<uint32_t>((kslot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = static_cast<uint32_t>(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+          const uint32_t off = static_cast<uint32_t>(
+              ((kk / C::kKPerBox) * C::kBoxBytes + (kk % C::kKPerBox) * 32) >> 4);
           ptx::mma_ss(tmem + t * kBN, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
         }
         ptx::tc_commit(bar_s_full + 8 * t);
@@ -291,7 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           ptx::mma_ts(tmem + C::kColO + t * D, tmem + t * kBN + kk * 8,
-                      dv + static_cast<uint32_t>(kk * 128), kIdescPV, kk > 0 ? 1u : acc);
+                      dv + static_cast<uint32_t>(kk * (16 * C::kRowBytes >> 4)), kIdescPV,
+                      kk > 0 ? 1u : acc);
         rec(tr::kPvIssued, (t << 16) | j);
       };
       uint32_t p_phase[kQTiles] = {0u, 0u};
@@ -480,7 +492,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld_32x32b_x32(tO + c0, o);
         ptx::tmem_wait_ld();
         ptx::reg_fence<32>(o);
-        tile::stage_bf16_sw128(stage, kBoxBytes, row, c0, o, inv_l);
+        if (D == 96)
+          tile::stage_bf16_sw64(stage, C::kBoxBytes, row, c0, o, inv_l);
+        else
+          tile::stage_bf16_sw128(stage, C::kBoxBytes, row, c0, o, inv_l);
       }
       ptx::fence_proxy_async_smem();
     }
@@ -488,7 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (do_store && quad == 0 && lane == 0) {
 #pragma unroll
       for (int bx = 0; bx < C::kBoxes; ++bx)
-        ptx::tma_store_4d(&tm_o, sQ + t * C::kTileBytes + bx * kBoxBytes, bx * 64, h, tq0, b);
+        ptx::tma_store_4d(&tm_o, sQ + t * C::kTileBytes + bx * C::kBoxBytes, bx * C::kBoxCols, h,
+                          tq0, b);
       ptx::tma_store_commit();
       ptx::tma_store_wait_read();
     }
@@ -518,10 +534,11 @@ cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* 
   // The maps carry the real head dim p.D <= D: loads zero-fill columns
   // p.D..D-1 (adding nothing to Q K^T and giving zero O columns) and the
   // store clips them.
-  if (!encode_bshd_tensor_map(&tq, q, p.B, p.S, p.H, p.D, p.sq, 1, kBM, p.cache_maps) ||
-      !encode_bshd_tensor_map(&tk, k, p.B, p.S, p.Hkv, p.D, p.sk, 1, kBN, p.cache_maps) ||
-      !encode_bshd_tensor_map(&tv, v, p.B, p.S, p.Hkv, p.D, p.sv, 1, kBN, p.cache_maps) ||
-      !encode_bshd_tensor_map(&to, out, p.B, p.S, p.H, p.D, p.so, 1, kBM, p.cache_maps))
+  constexpr int bc = Cfg<D>::kBoxCols;
+  if (!encode_bshd_tensor_map(&tq, q, p.B, p.S, p.H, p.D, p.sq, 1, kBM, p.cache_maps, bc) ||
+      !encode_bshd_tensor_map(&tk, k, p.B, p.S, p.Hkv, p.D, p.sk, 1, kBN, p.cache_maps, bc) ||
+      !encode_bshd_tensor_map(&tv, v, p.B, p.S, p.Hkv, p.D, p.sv, 1, kBN, p.cache_maps, bc) ||
+      !encode_bshd_tensor_map(&to, out, p.B, p.S, p.H, p.D, p.so, 1, kBM, p.cache_maps, bc))
     return cudaErrorInvalidValue;
   const int nqb = (p.S + kQTiles * kBM - 1) / (kQTiles * kBM);
   const long long grid = static_cast<long long>(nqb) * p.H * p.B;
@@ -542,9 +559,10 @@ int fwd_bf16_tc_ctas(int S) { return (S + kQTiles * kBM - 1) / (kQTiles * kBM); 
 
 cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, const void* k,
                                const void* v, cudaStream_t stream) {
-  // Head dims up to 64 (128) run on the 64 (128) column kernel.
+  // Head dims up to 64 (96, 128) run on the 64 (96, 128) column kernel.
   if (p.D % 8 != 0 || p.D < 8 || p.D > 128) return cudaErrorInvalidValue;
   if (p.D <= 64) return launch_d<64>(p, out, q, k, v, stream);
+  if (p.D <= 96) return launch_d<96>(p, out, q, k, v, stream);
   return launch_d<128>(p, out, q, k, v, stream);
   return cudaErrorInvalidValue;
 }

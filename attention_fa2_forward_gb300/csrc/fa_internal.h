@@ -135,14 +135,14 @@ unsigned long long wait_limit_ns();
 cudaError_t ensure_smem_attr(unsigned long long* done, const void* func, int bytes);
 
 // Encodes a 4-D BSHD tensor map (dims D, heads, S, B; element strides `st`,
-// D contiguous) for bf16 data with a {64, box_heads, box_rows, 1} box and
-// 128-byte swizzle. Returns false on failure. Maps are cached, keyed on every
+// D contiguous) for bf16 data with a {box_cols, box_heads, box_rows, 1} box:
+// 64 columns with the 128-byte swizzle, or 32 with the 64-byte swizzle. Returns false on failure. Maps are cached, keyed on every
 // argument (address, sizes, strides, box): a repeated call copies the cached
 // map instead of encoding it again; fa_shutdown() empties the cache. With
 // use_cache false the map is encoded and the cache neither read nor grown
 // (no host allocation).
 bool encode_bshd_tensor_map(CUtensorMap* map, const void* base, int B, int S, int heads, int D,
                             BshdStrides st, int box_heads = 1, int box_rows = 128,
-                            bool use_cache = true);
+                            bool use_cache = true, int box_cols = 64);
 
 }  // namespace fa

@@ -99,5 +99,26 @@ __device__ __forceinline__ void stage_bf16_sw128(uint8_t* stage, int box_bytes, 
   }
 }
 
+// As stage_bf16_sw128 for boxes of [rows][32 bf16] (64-byte rows) with the
+// 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3).
+// c0 is a multiple of 32: the 32 columns fill one box.
+__device__ __forceinline__ void stage_bf16_sw64(uint8_t* stage, int box_bytes, int row, int c0,
+                                                const uint32_t* o, float inv_l) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    uint4 pk;
+    pk.x = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l,
+                            __uint_as_float(o[8 * u + 1]) * inv_l);
+    pk.y = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l,
+                            __uint_as_float(o[8 * u + 3]) * inv_l);
+    pk.z = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l,
+                            __uint_as_float(o[8 * u + 5]) * inv_l);
+    pk.w = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l,
+                            __uint_as_float(o[8 * u + 7]) * inv_l);
+    const int phys = u ^ ((row >> 1) & 3);
+    *reinterpret_cast<uint4*>(stage + (c0 >> 5) * box_bytes + row * 64 + phys * 16) = pk;
+  }
+}
+
 }  // namespace tile
 }  // namespace fa

@@ -192,18 +192,29 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-// Shared-memory matrix descriptor for a 128B-swizzled operand tile whose
-// 8-row x 128-byte swizzle atoms start on a 1024-byte boundary.
+// Swizzle-mode field values of the tcgen05 shared-memory descriptor.
+constexpr uint32_t kSwizzle128B = 2;
+constexpr uint32_t kSwizzle64B = 4;
+
+// Shared-memory matrix descriptor for a swizzled operand tile whose 8-row
+// swizzle atoms (8 x 128 bytes for 128B, 8 x 64 bytes for 64B) start on an
+// atom-size boundary.
 //   lbo: byte distance between atoms along the leading dimension (used by
 //        MN-major operands), sbo: byte distance between 8-row groups.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swizzle_mode) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
-  d |= static_cast<uint64_t>(2) << 61;  // swizzle mode: 128B
+  d |= static_cast<uint64_t>(swizzle_mode & 7u) << 61;
   return d;
+}
+
+// The 128B-swizzled case (8-row x 128-byte atoms on a 1024-byte boundary).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(saddr, lbo, sbo, kSwizzle128B);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
