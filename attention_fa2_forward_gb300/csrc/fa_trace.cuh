@@ -37,7 +37,7 @@ namespace trace {
 // producer, MMA issuer, softmax warp 0 (tile 0) and 4 (tile 1), then softmax
 // warps 1, 2, 3, 5, 6, 7
 constexpr int kRoles = 10;
-constexpr int kEventsPerRole = 128;
+constexpr int kEventsPerRole = 256;
 constexpr int kRecordBytes = 16;
 constexpr unsigned long long kBytesPerCta =
     static_cast<unsigned long long>(kRoles) * kEventsPerRole * kRecordBytes;

@@ -49,32 +49,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// try_wait with a suspend-time hint: a thread that has to wait is suspended
-// for at most about `hint_ns` before the call returns false.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return done != 0;
-}
-
-// As mbar_wait, polling with short suspensions (hint_ns) so that a waiter on
-// the critical path resumes soon after the phase completes.
-__device__ __forceinline__ bool mbar_wait_hint(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                               uint32_t hint_ns) {
-  if (mbar_try_wait_hint(bar, parity, hint_ns)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_hint(bar, parity, hint_ns)) return true;
-    if ((it & 7u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
-  }
-}
-
 // Spin on try_wait until the phase completes or `limit_ns` of global time
 // pass. Returns false on time-out; never blocks longer than about the limit.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -255,22 +229,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
-}
-
-// 32 lanes x 8 consecutive 32-bit columns (thread t: lane t's row).
-__device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t* r) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t* r) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-                   taddr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
-               "r"(r[7])
-               : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

@@ -21,7 +21,7 @@ CODES = {1: "cta_start", 2: "q_load_issued", 3: "k_load_issued", 4: "v_load_issu
          5: "q_ready", 6: "s_issued", 7: "pv_issued", 8: "mma_drained", 9: "s_ready",
          10: "p_ready", 11: "epilogue_start", 12: "epilogue_end", 13: "s_loaded",
          14: "max_done", 15: "exp_done", 16: "p_seen"}
-EVENTS_PER_ROLE = 128
+EVENTS_PER_ROLE = 256
 
 
 def run_traced(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: float, mask="causal",

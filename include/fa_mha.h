@@ -348,10 +348,10 @@ int fa_version(void);
  * CTA, CTA c at offset c * fa_trace_bytes_per_cta(); CTAs past the buffer
  * record nothing. Each CTA holds 10 roles (TMA producer, MMA issuer, softmax
  * warps 0 and 4 -- the first of Q tile 0 and of Q tile 1 -- then softmax
- * warps 1, 2, 3, 5, 6, 7) x 128 records of 16 bytes: global timer
+ * warps 1, 2, 3, 5, 6, 7) x 256 records of 16 bytes: global timer
  * in ns (two 32-bit words), the SM's clock (low 32 bits), and event code <<
  * 24 | 24-bit argument; the codes are listed in csrc/fa_trace.cuh. A role's
- * records past 128 are dropped; records not written are left as they were
+ * records past 256 are dropped; records not written are left as they were
  * (zero the buffer first). NULL stops tracing. The default build returns
  * FA_ERR_UNSUPPORTED (and FA_OK for NULL).
  */

@@ -167,7 +167,7 @@ def test_debug_build_exports_the_same_symbols_and_traces():
     dbg = fa.load_debug_library()
     for name in _declared_functions():
         assert hasattr(dbg, name), name
-    assert dbg.fa_trace_bytes_per_cta() == 10 * 128 * 16
+    assert dbg.fa_trace_bytes_per_cta() == 10 * 256 * 16
     assert dbg.fa_trace_set_buffer(P + 8, 1 << 20) == fa.FA_ERR_INVALID_ARG  # 16-byte aligned
     assert dbg.fa_debug_set_lse_limit(-1) == fa.FA_ERR_INVALID_ARG
     assert dbg.fa_debug_set_lse_limit(0) == fa.FA_OK
