@@ -943,7 +943,7 @@ unsigned long long fa_trace_bytes_per_cta(void) { return FA_TRACE ? fa::trace::k
 
 long long fa_trace_ctas(int B, int S, int H, int D) {
   if (B < 1 || S < 1 || H < 1 || D < 8 || D > 128) return 0;
-  return static_cast<long long>(fa::fwd_bf16_tc_ctas(S)) * H * B;
+  return static_cast<long long>(fa::fwd_bf16_tc_ctas(S, D)) * H * B;
 }
 
 fa_status_t fa_debug_set_lse_limit(long long elems) {

@@ -8,18 +8,21 @@
 // sum l, unnormalised O rescaled by exp(m_old - m_new), one division by l at
 // the end), mapped onto Blackwell hardware:
 //
-//   * one CTA owns two 128-row Q tiles of one (b, h) and streams the K/V
-//     tiles both of them need through a shared-memory ring (TMA, 128-byte
-//     swizzle, straight from BSHD: the Step 0 / Step 4 transposes are the
-//     tensor maps' strides);
+//   * one CTA owns two 128-row Q tiles of one (b, h) -- or, for head dims up
+//     to 64 and sequences up to 1024, one Q tile, with two CTAs per SM -- and
+//     streams the K/V tiles
+//     they need through a shared-memory ring (TMA, swizzled, straight from
+//     BSHD: the Step 0 / Step 4 transposes are the tensor maps' strides);
 //   * S = Q K^T and O += P V are tcgen05.mma (bf16 in, fp32 accumulate) with
 //     S, P and O resident in tensor memory: S_t at columns [128t, 128t+128),
 //     P_t (bf16 pairs) written over the first 64 of them, O_t at
 //     [256 + D t, 256 + D (t+1));
 //   * warp roles: warps 0-3 and 4-7 are the softmax warpgroups of Q tile 0 and
-//     1 (thread = query row = TMEM lane), warp 8 issues the MMAs, warp 9 the
-//     TMA loads. The MMA order S0 S1 | PV0 S0' PV1 S1' | ... lets one tile's
-//     softmax overlap the other tile's MMAs;
+//     1 (thread = query row = TMEM lane), then one warp issues the MMAs and
+//     one the TMA loads. The MMA order S0 S1 | PV0 S0' PV1 S1' | ... lets one
+//     tile's softmax overlap the other tile's MMAs; with one Q tile per CTA
+//     the two CTAs on an SM overlap the same way, and one CTA's set-up and
+//     epilogue overlap the other's KV loop;
 //   * softmax in the log2 domain (exp2 of score * scale * log2 e minus the
 //     running max), with the rescale of O skipped while the running max grows
 //     by less than 2^8 (O and l keep the same stale max, so the final O / l is
@@ -51,12 +54,21 @@ namespace {
 
 constexpr int kBM = 128;                          // query rows per Q tile (= TMEM lanes)
 constexpr int kBN = tile::kBN;                    // keys per K/V tile
-constexpr int kQTiles = 2;                        // Q tiles per CTA
-constexpr int kSoftmaxWarps = 4 * kQTiles;        // one warpgroup per Q tile
-constexpr int kMmaWarp = kSoftmaxWarps;           // warp 8
-constexpr int kLoadWarp = kSoftmaxWarps + 1;      // warp 9
-constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
-constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxQTiles = 2;                     // Q tiles per CTA: QT = 1 or 2
+
+// Warp roles of a CTA with QT Q tiles: a softmax warpgroup per tile, then
+// the MMA warp and the TMA warp.
+template <int QT>
+struct Roles {
+  static constexpr int kSoftmaxWarps = 4 * QT;
+  static constexpr int kMmaWarp = kSoftmaxWarps;
+  static constexpr int kLoadWarp = kSoftmaxWarps + 1;
+  static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+  // One CTA of two tiles fills an SM's tensor memory; two CTAs of one tile
+  // share it (256 columns each: S 128, O up to 128).
+  static constexpr uint32_t kTmemCols = QT == 2 ? 512 : 256;
+  static constexpr int kCtasPerSm = 3 - QT;
+};
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr unsigned long long kDrainExtraNs = 100000000ull;  // 100 ms
@@ -65,9 +77,10 @@ constexpr unsigned long long kDrainExtraNs = 100000000ull;  // 100 ms
 // the 128-byte swizzle (D = 64, 128) or, for D = 96, of [128][32] with the
 // 64-byte swizzle (three boxes: the MMAs then run with K = 96 and N = 96, no
 // padding columns).
-template <int D>
+template <int D, int QT>
 struct Cfg {
   static_assert(D == 64 || D == 96 || D == 128, "head dim");
+  static_assert(QT == 2 || D <= 64, "one Q tile per CTA is built for D <= 64");
   static constexpr int kBoxCols = D == 96 ? 32 : 64;
   static constexpr int kRowBytes = kBoxCols * 2;          // bytes of one box row (= swizzle span)
   static constexpr int kBoxBytes = kBM * kRowBytes;
@@ -75,15 +88,18 @@ struct Cfg {
   static constexpr int kKPerBox = kBoxCols / 16;          // MMA K steps of 16 per box
   static constexpr uint32_t kSwizzle = D == 96 ? ptx::kSwizzle64B : ptx::kSwizzle128B;
   static constexpr int kTileBytes = kBoxes * kBoxBytes;  // one [128][D] bf16 tile
-  static constexpr int kStages = D == 128 ? 4 : 6;       // K/V ring slots
+  // K/V ring slots (one Q tile: small enough for two CTAs per SM)
+  static constexpr int kStages = QT == 1 ? 5 : (D == 128 ? 4 : 6);
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
+  static constexpr int kKVOff = kQOff + QT * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   // q_full[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] drain
   static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1 KB alignment
-  static constexpr uint32_t kColO = 256;                   // O_t at kColO + t * D
+  static constexpr uint32_t kColO = 128 * QT;              // O_t at kColO + t * D
+  static_assert(kColO + QT * D <= Roles<QT>::kTmemCols, "tensor memory");
+  static_assert(Roles<QT>::kCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024, "shared memory");
 };
 
 // Visibility bounds of query row i (keys lo..hi inclusive may be visible).
@@ -98,14 +114,19 @@ __device__ __forceinline__ RowBounds row_bounds(const FwdProblem& p, int i) {
   return r;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int QT>
+__global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
     fa_fwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_o, const FwdProblem p,
                           int num_qblocks) {
-  using C = Cfg<D>;
+  using C = Cfg<D, QT>;
+  constexpr int kSoftmaxWarps = Roles<QT>::kSoftmaxWarps;
+  constexpr int kMmaWarp = Roles<QT>::kMmaWarp;
+  constexpr int kLoadWarp = Roles<QT>::kLoadWarp;
+  constexpr uint32_t kTmemCols = Roles<QT>::kTmemCols;
+  (void)kSoftmaxWarps;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -141,12 +162,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = rem / p.H;
   const int hk = h / (p.H / p.Hkv);
 
-  // KV tile range [lo_t, hi_t) of each Q tile; empty when the tile is past S.
-  int q0[kQTiles], lo[kQTiles], hi[kQTiles];
+  // KV tile range [lo_t, hi_t) of each Q tile; empty when the tile is past S
+  // (and for tile 1 of a one-tile CTA).
+  int q0[kMaxQTiles], lo[kMaxQTiles], hi[kMaxQTiles];
 #pragma unroll
-  for (int t = 0; t < kQTiles; ++t) {
-    q0[t] = qb * (kQTiles * kBM) + t * kBM;
-    if (q0[t] < p.S) {
+  for (int t = 0; t < kMaxQTiles; ++t) {
+    q0[t] = qb * (QT * kBM) + t * kBM;
+    if (t < QT && q0[t] < p.S) {
       // Window without the causal mask: keys up to the last row + W - 1.
       const int kv_end = p.causal ? min(p.S, q0[t] + kBM)
                                   : (p.window > 0 ? min(p.S, q0[t] + kBM - 1 + p.window) : p.S);
@@ -164,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
 #pragma unroll
-    for (int t = 0; t < kQTiles; ++t) {
+    for (int t = 0; t < kMaxQTiles; ++t) {
       ptx::mbar_init(bar_q_full + 8 * t, 1);
       ptx::mbar_init(bar_s_full + 8 * t, 1);
       ptx::mbar_init(bar_p_full + 8 * t, 4);  // one arrival per softmax warp
@@ -205,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_q = ptx::policy_evict_first();
       const uint64_t pol_kv = ptx::policy_evict_last();
 #pragma unroll
-      for (int t = 0; t < kQTiles; ++t) {
+      for (int t = 0; t < QT; ++t) {
         if (lo[t] < hi[t]) {
           ptx::mbar_arrive_expect_tx(bar_q_full + 8 * t, C::kTileBytes);
 #pragma unroll
@@ -243,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Never leave while a copy of ours may still be writing shared memory.
 #pragma unroll
-      for (int t = 0; t < kQTiles; ++t)
+      for (int t = 0; t < QT; ++t)
         if (lo[t] < hi[t]) ptx::mbar_wait(bar_q_full + 8 * t, 0, drain_limit);
       for (int s = 0; s < C::kStages; ++s)
         if ((armed >> s) & 1u) ptx::mbar_wait(bar_kv_full + 8 * s, (armed_parity >> s) & 1u, drain_limit);
@@ -261,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
       }
 #pragma unroll
-      for (int t = 0; t < kQTiles; ++t)
+      for (int t = 0; t < QT; ++t)
         if (ok && lo[t] < hi[t] && !ptx::mbar_wait(bar_q_full + 8 * t, 0, limit)) {
           fail();
           ok = false;
@@ -306,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       kk > 0 ? 1u : acc);
         rec(tr::kPvIssued, (t << 16) | j);
       };
-      uint32_t p_phase[kQTiles] = {0u, 0u};
+      uint32_t p_phase[kMaxQTiles] = {0u, 0u};
       auto wait_p = [&](int t, int j) -> bool {
         if (aborted() || !ptx::mbar_wait(bar_p_full + 8 * t, p_phase[t], limit)) {
           fail();
@@ -324,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
         } else {
 #pragma unroll
-          for (int t = 0; t < kQTiles; ++t)
+          for (int t = 0; t < QT; ++t)
             if (in_tile(t, jlo)) issue_s(t, ks, jlo);
           ptx::tc_commit(bar_kv_empty + 8 * ks);
         }
@@ -345,14 +367,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ks < 0) break;
           if (in_tile(0, j + 1)) issue_s(0, ks, j + 1);
         }
-        if (in_tile(1, j)) {
+        if (QT > 1 && in_tile(1, j)) {
           if (!wait_p(1, j)) break;
           issue_pv(1, vs, j > lo[1], j);
           if (j == hi[1] - 1) ptx::tc_commit(bar_o_full + 8);
         }
         ptx::tc_commit(bar_kv_empty + 8 * vs);
         if (has_next) {
-          if (in_tile(1, j + 1)) issue_s(1, ks, j + 1);
+          if (QT > 1 && in_tile(1, j + 1)) issue_s(1, ks, j + 1);
           ptx::tc_commit(bar_kv_empty + 8 * ks);
         }
       }
@@ -527,44 +549,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, int QT>
 cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* k, const void* v,
                      cudaStream_t stream) {
+  using C = Cfg<D, QT>;
   CUtensorMap tq, tk, tv, to;
   // The maps carry the real head dim p.D <= D: loads zero-fill columns
   // p.D..D-1 (adding nothing to Q K^T and giving zero O columns) and the
   // store clips them.
-  constexpr int bc = Cfg<D>::kBoxCols;
+  constexpr int bc = C::kBoxCols;
   if (!encode_bshd_tensor_map(&tq, q, p.B, p.S, p.H, p.D, p.sq, 1, kBM, p.cache_maps, bc) ||
       !encode_bshd_tensor_map(&tk, k, p.B, p.S, p.Hkv, p.D, p.sk, 1, kBN, p.cache_maps, bc) ||
       !encode_bshd_tensor_map(&tv, v, p.B, p.S, p.Hkv, p.D, p.sv, 1, kBN, p.cache_maps, bc) ||
       !encode_bshd_tensor_map(&to, out, p.B, p.S, p.H, p.D, p.so, 1, kBM, p.cache_maps, bc))
     return cudaErrorInvalidValue;
-  const int nqb = (p.S + kQTiles * kBM - 1) / (kQTiles * kBM);
+  const int nqb = (p.S + QT * kBM - 1) / (QT * kBM);
   const long long grid = static_cast<long long>(nqb) * p.H * p.B;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
   static unsigned long long attr_done = 0;
   cudaError_t err = ensure_smem_attr(&attr_done, reinterpret_cast<const void*>(
-                                                     &fa_fwd_bf16_tc_kernel<D>),
-                                     Cfg<D>::kSmemBytes);
+                                                     &fa_fwd_bf16_tc_kernel<D, QT>),
+                                     C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  fa_fwd_bf16_tc_kernel<D><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(
-      tq, tk, tv, to, p, nqb);
+  fa_fwd_bf16_tc_kernel<D, QT><<<static_cast<unsigned>(grid), Roles<QT>::kThreads, C::kSmemBytes,
+                                 stream>>>(tq, tk, tv, to, p, nqb);
   return cudaGetLastError();
 }
 
+// Q tiles per CTA: one for head dims up to 64 and sequences up to 1024 --
+// a CTA of one tile fits twice on an SM, and on short sequences, whose tiles
+// see few KV steps, one CTA's set-up and epilogue then overlap the other's
+// work (B4 H16 S1024 D64 causal: 280 -> 302 TFLOP/s; B8 S512: 174 -> 204) --
+// else two (one-tile CTAs lose ~4 % on S >= 2048).
+int q_tiles_per_cta(int D, int S) { return D <= 64 && S <= 1024 ? 1 : 2; }
+
 }  // namespace
 
-int fwd_bf16_tc_ctas(int S) { return (S + kQTiles * kBM - 1) / (kQTiles * kBM); }
+int fwd_bf16_tc_ctas(int S, int D) {
+  const int rows = q_tiles_per_cta(D, S) * kBM;
+  return (S + rows - 1) / rows;
+}
 
 cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, const void* k,
                                const void* v, cudaStream_t stream) {
   // Head dims up to 64 (96, 128) run on the 64 (96, 128) column kernel.
   if (p.D % 8 != 0 || p.D < 8 || p.D > 128) return cudaErrorInvalidValue;
-  if (p.D <= 64) return launch_d<64>(p, out, q, k, v, stream);
-  if (p.D <= 96) return launch_d<96>(p, out, q, k, v, stream);
-  return launch_d<128>(p, out, q, k, v, stream);
-  return cudaErrorInvalidValue;
+  if (p.D <= 64)
+    return q_tiles_per_cta(p.D, p.S) == 1 ? launch_d<64, 1>(p, out, q, k, v, stream)
+                                          : launch_d<64, 2>(p, out, q, k, v, stream);
+  if (p.D <= 96) return launch_d<96, 2>(p, out, q, k, v, stream);
+  return launch_d<128, 2>(p, out, q, k, v, stream);
 }
 
 }  // namespace fa

@@ -76,8 +76,9 @@ cudaError_t launch_decode_bf16_tc(const DecodeProblem& p, void* out, const void*
 // 16-byte-aligned dense BSHD / BShD bf16 tensors. Returns a cudaError_t.
 cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, const void* k,
                                const void* v, cudaStream_t stream);
-// Query blocks (CTAs per (batch, head)) of that kernel for S queries.
-int fwd_bf16_tc_ctas(int S);
+// Query blocks (CTAs per (batch, head)) of that kernel for S queries and
+// head dim D.
+int fwd_bf16_tc_ctas(int S, int D);
 
 // CUDA-core fp32 forward for fp32 tensors.
 cudaError_t launch_fwd_f32_simt(const FwdProblem& p, float* out, const float* q, const float* k,

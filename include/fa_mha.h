@@ -362,8 +362,9 @@ unsigned long long fa_trace_bytes_per_cta(void);
 
 /*
  * fa_trace_ctas -- CTAs of one bf16 prefill launch (D <= 128) for these
- * sizes: one per (256-query block, head, batch); 0 for sizes that launch
- * another kernel.
+ * sizes: one per (query block, head, batch), blocks of 128 queries for D up
+ * to 64 with S up to 1024, else of 256; 0 for sizes that launch another
+ * kernel.
  */
 long long fa_trace_ctas(int B, int S, int H, int D);
 

@@ -47,6 +47,7 @@ def _kv_tiles(q0, S, causal, window):
 @pytest.mark.parametrize("B,S,H,Hkv,D,causal,window", [
     (2, 1000, 4, 2, 128, True, -1),
     (1, 1500, 4, 4, 64, False, -1),
+    (2, 900, 4, 2, 64, True, -1),
     (1, 2100, 2, 1, 128, True, 300),
     (1, 700, 2, 2, 64, False, 200),
 ])
@@ -63,7 +64,8 @@ def test_trace_matches_the_launch(B, S, H, Hkv, D, causal, window):
     assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
 
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    nqb = (S + 255) // 256
+    tiles = 1 if D <= 64 and S <= 1024 else 2  # Q tiles of 128 rows per CTA
+    nqb = (S + 128 * tiles - 1) // (128 * tiles)
     assert len(events) == nqb * H * B
     eff_window = window if 0 < window < S else -1
     for e in events:
@@ -77,8 +79,8 @@ def test_trace_matches_the_launch(B, S, H, Hkv, D, causal, window):
         for t_ns, _, code, arg in e["roles"]["mma"]:
             if code == "s_issued":
                 s_issued[(arg >> 16, arg & 0xFFFF)] = t_ns
-        for t in range(2):
-            lo, hi = _kv_tiles(qb * 256 + t * 128, S, causal, eff_window)
+        for t in range(tiles):
+            lo, hi = _kv_tiles(qb * 128 * tiles + t * 128, S, causal, eff_window)
             ready = [(t_ns, arg) for t_ns, _, code, arg in e["roles"][f"softmax{t}"]
                      if code == "s_ready"]
             assert [a for _, a in ready] == list(range(lo, hi)), (c, t)
