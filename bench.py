@@ -234,9 +234,15 @@ class ClockSampler:
             time.sleep(self.period)
 
     def start(self):
+        """Start sampling and return once the first sample is in, so that the
+        thread's start-up (NVML's first calls) falls before the timed region
+        rather than inside its first step."""
         if self.ok:
             self._thread = threading.Thread(target=self._run, daemon=True)
             self._thread.start()
+            t0 = time.perf_counter()
+            while not self.samples and time.perf_counter() - t0 < 0.2:
+                time.sleep(0.001)
 
     def stop(self):
         if self.ok and self._thread is not None:
