@@ -301,9 +301,10 @@ def mha_no_cache_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: to
 
 def kv_cache_plan(B: int, Sq: int, S_cache: int, H: int, Hkv: int, D: int, mask="causal",
                   window: int = -1, num_splits: int = 0, num_sms: int = 0) -> tuple[int, int]:
-    """(splits, workspace bytes) that :func:`mha_kv_cache` uses for these sizes.
-    ``num_sms`` = 0 plans for the current device; n > 0 for an n-SM device
-    (no CUDA call)."""
+    """(splits, workspace bytes) that :func:`mha_kv_cache` uses for these sizes:
+    splits = 1 when every unit runs whole, else the most pieces one unit can
+    be cut into. ``num_sms`` = 0 plans for the current device; n > 0 for an
+    n-SM device (no CUDA call)."""
     if num_sms == 0:
         num_sms = _sm_count(torch.cuda.current_device())
     return _kv_cache_plan(int(B), int(Sq), int(S_cache), int(H), int(Hkv), int(D),
@@ -338,9 +339,11 @@ def mha_kv_cache(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     values (cache_lens: int32 CUDA tensor [B], or None for full caches). Query
     row s of batch b sits at position cache_lens[b] - Sq + s; the mask is
     evaluated there. All tensors contiguous bf16. ``num_splits`` = 0 lets the
-    library pick the key-range split; the workspace it needs is allocated here
-    unless given. Returns out [B, Sq, H, D] (and lse [B, H, Sq] fp32 if
-    ``return_lse``).
+    library share out the work (few (batch, KV head, position tile) units:
+    equal quotas of all units' key tiles per persistent CTA, found from
+    cache_lens on the device); n >= 1 cuts every unit into n even key ranges.
+    The workspace it needs is allocated here unless given. Returns out
+    [B, Sq, H, D] (and lse [B, H, Sq] fp32 if ``return_lse``).
     """
     if q.dim() != 4 or k_cache.dim() != 4 or v_cache.dim() != 4:
         raise ValueError("q, k_cache, v_cache must be 4-D (BSHD)")

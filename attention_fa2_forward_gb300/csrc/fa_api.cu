@@ -405,10 +405,18 @@ struct KvPlan {
   int G, Pq, R, n_ptiles;
   int window;  // effective window (0: none)
   int splits, tiles_per_split;
+  int ctas;          // persistent CTAs (0: a CTA per unit)
+  int stream_k_min;  // > 0: stream-K sharing, quotas of at least this many tiles
   unsigned long long o_part_bytes, workspace_bytes;
 };
 
 constexpr int kMaxSplits = 128;
+// Stream-K sharing: persistent CTAs per SM count (27/32: 128 of 152 SMs) --
+// on a 152-SM GB300 the streaming CTAs' aggregate HBM throughput peaks at
+// 128 CTAs and falls past it (one 131072-key cache, 8 KV heads: 6.1 TB/s at
+// 128, 5.7 at 152) -- and the smallest quota in KV tiles.
+constexpr long long kStreamKCtasNum = 27, kStreamKCtasDen = 32;
+constexpr int kStreamKMinTiles = 2;
 
 unsigned long long align256(unsigned long long x) { return (x + 255ull) & ~255ull; }
 
@@ -455,37 +463,61 @@ KvPlan make_kv_plan(int B, int Sq, int S_cache, int H, int Hkv, int D, int causa
     max_tiles = (span + 127) / 128 + 1;
     if (max_tiles > all_tiles) max_tiles = all_tiles;
   }
-  long long splits = num_splits;
-  if (splits == 0) {
+  const long long units = static_cast<long long>(B) * Hkv * k.n_ptiles;
+  const unsigned long long d_pad = padded_head_dim(D);  // the kernel's padded row
+  unsigned long long slots = 0;                          // partial-result slots of R rows
+  if (num_splits == 0) {
     // Auto. Units (batch x KV head x position tile) that fill half the SMs
-    // stream best unsplit (one CTA each, no combine). Fewer units are cut:
-    //  * very few (at most one per 8 SMs: a few long sequences) into about
-    //    0.75 x SMs CTAs -- one CTA per SM streams about 54 GB/s, and past
-    //    ~128 concurrent streams the HBM gives each less than the extra
-    //    streams add (14 splits of one 131072-key sequence: 89 % of the HBM
-    //    peak, 19: 82 %, 22, a second wave of 24 CTAs: 65 %);
-    //  * more, whose lengths may be ragged (unknown here: they live on the
-    //    device), into about two CTAs per SM, so that the splits of short
-    //    sequences finish early and free their SMs for the long ones.
-    const long long units = static_cast<long long>(B) * Hkv * k.n_ptiles;
-    if (2 * units >= num_sms) {
-      splits = 1;
-    } else if (8 * units <= num_sms) {
-      splits = (3ll * num_sms) / (4 * units);
-      if (splits < 1) splits = 1;
+    // stream best whole (one CTA each, no combine). Fewer are shared out
+    // stream-K fashion: every persistent CTA takes an equal quota of all the
+    // units' KV tiles (the lengths, and so the total, are known only on the
+    // device); a unit is cut at the quota boundaries inside it.
+    if (2 * units >= num_sms || max_tiles <= kStreamKMinTiles) {
+      k.splits = 1;
+      k.tiles_per_split = static_cast<int>(max_tiles);
+    } else if (units / Hkv > fa::kDecodeMaxItems) {
+      // More position-tile groups than a CTA's item list holds (a device with
+      // many SMs): fixed splits, about two per SM.
+      num_splits = static_cast<int>((2ll * num_sms + units - 1) / units);
+      if (num_splits < 2) num_splits = 2;
     } else {
-      splits = (2ll * num_sms + units / 2) / units;  // rounded
+      // CTA groups of Hkv CTAs (one per KV head) share each quota.
+      long long ctas = (kStreamKCtasNum * num_sms) / kStreamKCtasDen / Hkv * Hkv;
+      if (ctas < Hkv) ctas = Hkv;
+      k.ctas = static_cast<int>(ctas);
+      k.stream_k_min = kStreamKMinTiles;
+      k.tiles_per_split = static_cast<int>(max_tiles);
+      // Pieces one unit may be cut into: one per CTA group at most, one per
+      // tile.
+      const long long groups_of_ctas = ctas / Hkv;
+      k.splits = static_cast<int>(groups_of_ctas < max_tiles ? groups_of_ctas : max_tiles);
+      if (k.splits < 2) k.splits = 2;
+      // Pieces in all: one per unit with keys, plus one per unit of a group
+      // that a quota boundary cuts.
+      slots = static_cast<unsigned long long>(units + ctas);
     }
   }
-  if (splits > kMaxSplits) splits = kMaxSplits;
-  if (splits > max_tiles) splits = max_tiles;
-  k.tiles_per_split = static_cast<int>((max_tiles + splits - 1) / splits);
-  k.splits = static_cast<int>((max_tiles + k.tiles_per_split - 1) / k.tiles_per_split);
-  if (k.splits > 1) {
-    const unsigned long long rows = static_cast<unsigned long long>(B) * Sq * H;
-    const unsigned long long d_pad = padded_head_dim(D);  // the kernel's padded row
-    k.o_part_bytes = align256(k.splits * rows * d_pad * 4ull);
-    k.workspace_bytes = k.o_part_bytes + align256(k.splits * rows * 4ull);
+  if (num_splits > 0) {
+    // Fixed splits: the unit's tiles cut in `splits` even ranges; persistent
+    // CTAs (one per SM at most) take every CTA-count-th range with keys.
+    long long splits = num_splits;
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    if (splits > max_tiles) splits = max_tiles;
+    k.tiles_per_split = static_cast<int>((max_tiles + splits - 1) / splits);
+    k.splits = static_cast<int>((max_tiles + k.tiles_per_split - 1) / k.tiles_per_split);
+    if (k.splits > 1) {
+      // One CTA per SM; more when a CTA's share would not fit its list.
+      const long long ranges = units * k.splits;
+      long long ctas = ranges < num_sms ? ranges : num_sms;
+      const long long need = (ranges + fa::kDecodeMaxItems - 1) / fa::kDecodeMaxItems;
+      if (ctas < need) ctas = need;
+      k.ctas = static_cast<int>(ctas);
+      slots = static_cast<unsigned long long>(ranges);
+    }
+  }
+  if (slots > 0) {
+    k.o_part_bytes = align256(slots * k.R * d_pad * 4ull);
+    k.workspace_bytes = k.o_part_bytes + align256(slots * k.R * 4ull);
   }
   return k;
 }
@@ -708,6 +740,7 @@ fa_status_t fa_mha_kv_cache(void* out, float* lse, const void* q, const void* k_
   if (plan.workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < plan.workspace_bytes))
     return fail(FA_ERR_INVALID_ARG, "workspace of %llu bytes needed (%d splits), %llu given",
                 plan.workspace_bytes, plan.splits, workspace != nullptr ? workspace_bytes : 0ull);
+  // Units (a CTA each when unsplit) and partial slots must be indexable.
   if (static_cast<long long>(plan.splits) * Hkv * plan.n_ptiles * B > 0x7fffffffll)
     return fail(FA_ERR_UNSUPPORTED, "problem too large (grid)");
   unsigned* status = nullptr;
@@ -731,6 +764,8 @@ fa_status_t fa_mha_kv_cache(void* out, float* lse, const void* q, const void* k_
   p.lens = cache_lens;
   p.splits = plan.splits;
   p.tiles_per_split = plan.tiles_per_split;
+  p.persistent = plan.splits > 1 ? plan.ctas : 0;
+  p.stream_k_min = plan.stream_k_min;
   p.lse = lse;
   if (plan.splits > 1) {
     p.o_part = static_cast<float*>(workspace);

@@ -50,8 +50,17 @@ struct FwdProblem {
 // Attention over a KV cache (bf16, tensor cores): batch b holds L_b keys at
 // the start of a [B, Scache, Hkv, D] cache; its Sq queries ([B, Sq, H, D])
 // sit at positions L_b - Sq .. L_b - 1. A Q tile packs Pq positions x G heads
-// of one KV head (R = G * Pq <= 128 rows); each (b, KV head, position tile)
-// is cut into `splits` ranges of `tiles_per_split` KV tiles.
+// of one KV head (R = G * Pq <= 128 rows); a unit is one (b, KV head,
+// position tile). Three ways to share out the units' KV tiles:
+//   persistent = 0: a CTA per unit, each unit whole (no partial results);
+//   persistent = C > 0, stream_k_min = 0: C CTAs; each unit is cut into
+//     `splits` ranges of `tiles_per_split` tiles and the CTAs take every C-th
+//     of the ranges that hold keys;
+//   persistent = C > 0, stream_k_min > 0: C CTAs take equal contiguous
+//     quotas (at least stream_k_min tiles) of all units' tiles laid end to
+//     end, found from the lengths on the device.
+// In the last two, each piece of a unit writes its partial O / l and LSE to a
+// slot of R rows; a second kernel merges each unit's slots.
 struct DecodeProblem {
   int B, Sq, Scache, H, Hkv, D;
   int G, Pq, R, n_ptiles;  // tile geometry
@@ -59,14 +68,20 @@ struct DecodeProblem {
   float scale, scale_log2;
   const int* lens;         // [B] keys per batch (clamped to [0, Scache]) or nullptr: Scache
   int splits, tiles_per_split;
+  int persistent;
+  int stream_k_min;
   float* lse;              // [B, H, Sq] fp32 or nullptr
-  float* o_part;           // [splits, B, Sq, H, D] fp32 partial O / l (splits > 1)
-  float* lse_part;         // [splits, B, H, Sq] fp32 partial LSE (splits > 1)
+  float* o_part;           // [slots, R, D] fp32 partial O / l (split modes)
+  float* lse_part;         // [slots, R] fp32 partial LSE (split modes)
   unsigned* status;
   unsigned long long wait_limit_ns;
   int stall_probe;
   BshdStrides sq, sk, sv, so;  // layouts of q, the caches and out (zero: dense)
 };
+
+// Items (unit, KV-tile range, slot) one CTA of the KV-cache kernel can hold
+// in its list; the plan keeps every CTA's share within it.
+constexpr int kDecodeMaxItems = 80;
 
 // Launches the KV-cache kernel (and, with splits > 1, the combine kernel).
 cudaError_t launch_decode_bf16_tc(const DecodeProblem& p, void* out, const void* q, const void* k,

@@ -18,6 +18,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Programmatic dependent launch: once every CTA of this grid has called
+// launch_dependents (or exited), the next kernel of the stream, if launched
+// with programmatic stream serialization, may start; that kernel calls
+// grid_dependency_wait before it touches this grid's results (the wait
+// returns once this grid has completed and its writes are visible, and at
+// once when there is no such grid).
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -226,8 +226,16 @@ unsigned long long fa_mha_no_cache_f32_tc_workspace(int B, int S, int Hkv, int D
  *   B, Sq, S_cache, H, Hkv, D : sizes; all >= 1, H % Hkv == 0,
  *             H / Hkv <= 128, D a multiple of 8 up to 256.
  *   scale, mask_kind, local_window_size : as fa_mha_no_cache.
- *   num_splits : 0 picks the number of key-range splits from the device's SM
- *             count; n >= 1 asks for n (capped at the number of key tiles).
+ *   num_splits : 0 lets the library share out the work. A unit is one
+ *             (batch, KV head, position tile of up to 128 / (H / Hkv)
+ *             queries). Units that fill half the SMs run whole, one CTA each.
+ *             Fewer units are shared out stream-K fashion: groups of Hkv
+ *             persistent CTAs (one per KV head, 27/32 of the SMs in all)
+ *             take equal contiguous quotas of all units' key tiles, found
+ *             from cache_lens on the device, and a unit is cut where a quota
+ *             ends. n >= 1 asks for n even key ranges per unit (capped at
+ *             the number of key tiles and at 128), which persistent CTAs
+ *             share round-robin. Cut units are merged by a second kernel.
  *   workspace, workspace_bytes : caller-owned device scratch of at least the
  *             size fa_mha_kv_cache_plan returns for the same arguments (may be
  *             NULL when that size is 0); 16-byte aligned.
@@ -246,8 +254,11 @@ fa_status_t fa_mha_kv_cache(void *out, float *lse, const void *q, const void *k_
 
 /*
  * fa_mha_kv_cache_plan -- how fa_mha_kv_cache will cut the work for these
- * arguments: *splits_out receives the number of key-range splits and
- * *workspace_bytes_out the scratch it needs (0 when there is one split).
+ * arguments: *splits_out receives 1 when every unit runs whole, else the
+ * most pieces one unit can be cut into (the requested ranges, or the number
+ * of CTA groups of the stream-K plan); *workspace_bytes_out the scratch it
+ * needs (0 when every unit runs whole: fp32 partial O rows and LSEs, one slot
+ * of H / Hkv x (position-tile) rows per piece).
  * num_sms = 0 uses the current device's SM count (the one fa_mha_kv_cache
  * uses); n >= 1 plans for a device with n SMs and makes no CUDA call.
  */

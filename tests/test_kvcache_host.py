@@ -30,11 +30,30 @@ def _expected_splits(req, tiles):
     return -(-tiles // per)
 
 
-def test_auto_split_requests_of_the_decode_workloads():
-    # one 131072-key sequence x 8 KV heads: 14 splits (112 CTAs); a ragged
-    # batch of 8 x 8 KV heads: 5 (320 CTAs, short splits finish early)
-    assert _plan(1, 1, 131072, 32, 8, 128)[0] == 14
-    assert _plan(8, 4, 32768, 32, 8, 128)[0] == 5
+def _ws(slots, R, d_pad=128):
+    """Workspace of `slots` partial slots of R rows: fp32 O rows, then LSEs."""
+    return ((slots * R * d_pad * 4 + 255) // 256 * 256) + ((slots * R * 4 + 255) // 256 * 256)
+
+
+def _auto(units, tiles, R, Hkv, sms=152):
+    """The automatic plan: units that fill half the SMs (or caches of at most
+    two tiles) run whole; fewer are shared out stream-K fashion over groups of
+    Hkv CTAs (27/32 x SMs CTAs in all), a unit cut into at most one piece per
+    CTA group; one partial slot per unit plus one per CTA."""
+    if 2 * units >= sms or tiles <= 2:
+        return 1, 0
+    ctas = max(Hkv, 27 * sms // 32 // Hkv * Hkv)
+    return max(2, min(ctas // Hkv, tiles)), _ws(units + ctas, R)
+
+
+def test_auto_plan_of_the_decode_workloads():
+    # one 131072-key sequence x 8 KV heads (G = 4, one position: R = 4 rows);
+    # a ragged batch of 8 x 8 KV heads, 4 positions (R = 16): both stream-K
+    # over 128 CTAs in 16 groups of 8 (one per KV head)
+    assert _plan(1, 1, 131072, 32, 8, 128) == (16, _ws(8 + 128, 4))
+    assert _plan(8, 4, 32768, 32, 8, 128) == (16, _ws(64 + 128, 16))
+    assert _plan(1, 1, 131072, 32, 8, 128, num_sms=76) == (8, _ws(8 + 64, 4))
+    assert _plan(1, 1, 131072, 24, 3, 128) == _auto(3, 1024, 8, 3)  # 126 CTAs
 
 
 def test_enough_units_take_one_split():
@@ -43,36 +62,25 @@ def test_enough_units_take_one_split():
     assert _plan(16, 1, 8192, 32, 8, 128) == (1, 0)
     assert _plan(19, 1, 8192, 16, 4, 128) == (1, 0)
     assert _plan(37, 1, 8192, 8, 2, 128)[0] > 1
-
-
-def _auto_request(units, sms=152):
-    """The automatic split request: a few long units into ~0.75 x SMs CTAs,
-    more units into ~2 CTAs per SM (rounded)."""
-    if 2 * units >= sms:
-        return 1
-    if 8 * units <= sms:
-        return max(1, 3 * sms // (4 * units))
-    return (2 * sms + units // 2) // units
+    # caches of two tiles or fewer are not shared out
+    assert _plan(1, 1, 256, 8, 2, 128) == (1, 0)
 
 
 @pytest.mark.parametrize("B,Hkv,S", [(1, 8, 131072), (2, 8, 32768), (1, 1, 65536), (4, 4, 8192),
                                      (8, 8, 32768)])
-def test_few_units_are_split_to_fill_the_gpu(B, Hkv, S):
-    splits, ws = _plan(B, 1, S, 8 * Hkv, Hkv, 128)
-    units = B * Hkv
-    assert splits == _expected_splits(_auto_request(units), _tiles(S))
-    rows = B * 8 * Hkv
-    expect = ((splits * rows * 128 * 4 + 255) // 256 * 256) + ((splits * rows * 4 + 255) // 256 * 256)
-    assert ws == expect
+def test_few_units_are_shared_out(B, Hkv, S):
+    assert _plan(B, 1, S, 8 * Hkv, Hkv, 128) == _auto(B * Hkv, _tiles(S), 8, Hkv)
 
 
 @pytest.mark.parametrize("req", [1, 2, 3, 7, 64, 200])
 def test_requested_splits_are_capped_and_cover_every_tile(req):
     S = 5000
-    splits, _ = _plan(1, 1, S, 8, 2, 128, num_splits=req)
+    splits, ws = _plan(1, 1, S, 8, 2, 128, num_splits=req)
     tiles = _tiles(S)
     assert 1 <= splits <= min(req, 128, tiles)
     assert splits == _expected_splits(req, tiles)  # no trailing split without tiles
+    # one slot of R = 4 rows per (unit, split)
+    assert ws == (0 if splits == 1 else _ws(2 * splits, 4))
 
 
 def test_window_bounds_the_tiles_to_split():
@@ -84,11 +92,12 @@ def test_window_bounds_the_tiles_to_split():
 
 
 def test_position_tiles_count_as_units():
-    # Sq = 64 with 4 heads per KV head: 2 position tiles of 32 positions.
-    s1, _ = _plan(1, 64, 16384, 8, 2, 128)
-    s2, _ = _plan(1, 32, 16384, 8, 2, 128)
-    assert s1 == _expected_splits(_auto_request(4), 128)   # 2 KV heads x 2 position tiles
-    assert s2 == _expected_splits(_auto_request(2), 128)
+    # Sq = 64 with 4 heads per KV head: 2 position tiles of 32 positions
+    # (R = 128 rows); Sq = 32: one.
+    assert _plan(1, 64, 16384, 8, 2, 128) == _auto(4, 128, 128, 2)
+    assert _plan(1, 32, 16384, 8, 2, 128) == _auto(2, 128, 128, 2)
+    # 40 batches x 2 KV heads x 2 position tiles fill half of 152 SMs
+    assert _plan(40, 64, 16384, 8, 2, 128) == (1, 0)
 
 
 P = 0x10000  # a non-null, 16-byte aligned fake address: never dereferenced
