@@ -79,9 +79,14 @@ struct UnitRange {
   int L, sq0, nq, pos0, t0, t1;
 };
 
-__device__ __forceinline__ UnitRange unit_range(const DecodeProblem& p, int pt, int b) {
+// Keys of batch b (clamped into [0, Scache]).
+__device__ __forceinline__ int batch_len(const DecodeProblem& p, int b) {
+  return min(max(p.lens != nullptr ? p.lens[b] : p.Scache, 0), p.Scache);
+}
+
+__device__ __forceinline__ UnitRange unit_range_of(const DecodeProblem& p, int pt, int L) {
   UnitRange u;
-  u.L = min(max(p.lens != nullptr ? p.lens[b] : p.Scache, 0), p.Scache);
+  u.L = L;
   u.sq0 = pt * p.Pq;              // first query row of the tile
   u.nq = min(p.Pq, p.Sq - u.sq0);  // query positions in the tile
   u.pos0 = u.L - p.Sq + u.sq0;     // position of the first of them
@@ -96,6 +101,10 @@ __device__ __forceinline__ UnitRange unit_range(const DecodeProblem& p, int pt, 
     u.t1 = khi / kBN + 1;
   }
   return u;
+}
+
+__device__ __forceinline__ UnitRange unit_range(const DecodeProblem& p, int pt, int b) {
+  return unit_range_of(p, pt, batch_len(p, b));
 }
 
 // Units are numbered (position-tile group, KV head) with the KV head fastest:
@@ -141,9 +150,10 @@ __device__ __forceinline__ long long unit_pieces(long long P, long long T, long 
   return T > 0 ? (P + T - 1) / q - P / q + 1 : 0;
 }
 
-// One entry of a CTA's item list: unit, KV tiles [jlo, jhi), partial slot.
+// One entry of a CTA's item list: unit, KV tiles [jlo, jhi), partial slot,
+// and the batch's key count (so that no role reads the lengths again).
 struct ItemRef {
-  int unit, jlo, jhi, piece;
+  int unit, jlo, jhi, piece, L;
 };
 constexpr int kMaxItems = kDecodeMaxItems;  // list capacity (the plan sizes the work to fit)
 
@@ -152,10 +162,11 @@ __device__ __forceinline__ Item load_item(const DecodeProblem& p, const ItemRef&
   const int grp = r.unit / p.Hkv;
   const int pt = group_pt(p, grp);
   const int b = grp / p.n_ptiles;
-  return make_item(p, unit_range(p, pt, b), hk, pt, b, r.jlo, r.jhi, r.piece);
+  return make_item(p, unit_range_of(p, pt, r.L), hk, pt, b, r.jlo, r.jhi, r.piece);
 }
 
-// The items of this CTA, in order (one thread):
+// The items of this CTA, in order (lane 0 of warp 0 builds the list; the
+// other lanes return 0):
 //   grid mode: unit blockIdx.x, whole (also without keys: its rows get O = 0);
 //   fixed splits: every gridDim.x-th of the units' `splits` ranges that hold
 //     keys, slot unit * splits + split;
@@ -163,21 +174,26 @@ __device__ __forceinline__ Item load_item(const DecodeProblem& p, const ItemRef&
 //     overlap for this CTA's KV head; slot base * Hkv + hk * pieces + k, with
 //     base = the pieces of the groups before, k = this quota's index among
 //     those the group touches.
-__device__ __noinline__ int build_items(const DecodeProblem& p, ItemRef* list) {
+// (A warp-parallel version of this list, lane per group, measured 12 %
+// slower on fixed splits although it built the same lists.)
+__device__ __noinline__ int build_items(const DecodeProblem& p, ItemRef* list, int lane) {
+  if (lane != 0) return 0;
   const int g = static_cast<int>(blockIdx.x);
   if (p.persistent == 0) {
     const int grp = g / p.Hkv;
-    const UnitRange u = unit_range(p, group_pt(p, grp), grp / p.n_ptiles);
-    list[0] = ItemRef{g, u.t0, u.t1, 0};
+    const int L = batch_len(p, grp / p.n_ptiles);
+    const UnitRange u = unit_range_of(p, group_pt(p, grp), L);
+    list[0] = ItemRef{g, u.t0, u.t1, 0, L};
     return 1;
   }
   const int groups = p.n_ptiles * p.B;
   int count = 0;
   if (p.stream_k_min == 0) {
     const long long C = gridDim.x;
-    long long i = g;  // next range (split * Hkv + hk) of the group
+    long long i = g;
     for (int grp = 0; grp < groups && count < kMaxItems; ++grp) {
-      const UnitRange u = unit_range(p, group_pt(p, grp), grp / p.n_ptiles);
+      const int L = batch_len(p, grp / p.n_ptiles);
+      const UnitRange u = unit_range_of(p, group_pt(p, grp), L);
       const long long ns = (u.t1 - u.t0 + p.tiles_per_split - 1) / p.tiles_per_split;
       const long long nk = ns * p.Hkv;
       for (; i < nk && count < kMaxItems; i += C) {
@@ -186,7 +202,7 @@ __device__ __noinline__ int build_items(const DecodeProblem& p, ItemRef* list) {
         const int jlo = u.t0 + split * p.tiles_per_split;
         const int unit = grp * p.Hkv + hk;
         list[count++] = ItemRef{unit, jlo, min(u.t1, jlo + p.tiles_per_split),
-                                unit * p.splits + split};
+                                unit * p.splits + split, L};
       }
       i -= nk;
     }
@@ -202,7 +218,8 @@ __device__ __noinline__ int build_items(const DecodeProblem& p, ItemRef* list) {
   const long long lo = static_cast<long long>(g / p.Hkv) * q, hi = lo + q;
   long long P = 0, base = 0;
   for (int grp = 0; grp < groups && P < hi && count < kMaxItems; ++grp) {
-    const UnitRange u = unit_range(p, group_pt(p, grp), grp / p.n_ptiles);
+    const int L = batch_len(p, grp / p.n_ptiles);
+    const UnitRange u = unit_range_of(p, group_pt(p, grp), L);
     const long long T = u.t1 - u.t0;
     const long long a = lo > P ? lo : P;
     const long long e = hi < P + T ? hi : P + T;
@@ -211,7 +228,7 @@ __device__ __noinline__ int build_items(const DecodeProblem& p, ItemRef* list) {
       const long long k = g / p.Hkv - P / q;
       list[count++] = ItemRef{grp * p.Hkv + hk, u.t0 + static_cast<int>(a - P),
                               u.t0 + static_cast<int>(e - P),
-                              static_cast<int>(base * p.Hkv + hk * pieces + k)};
+                              static_cast<int>(base * p.Hkv + hk * pieces + k), L};
     }
     base += pieces;
     P += T;
@@ -233,7 +250,7 @@ struct DCfg {
   // Ring slots: what fits next to the Q area in 227 KB. Two slots suffice for
   // the ring order (K0 K1 | V0 K2 | ...): each refill waits only on an MMA
   // that needs nothing later in the ring.
-  static constexpr int kStages = D == 256 ? 2 : (D == 128 ? 6 : 12);
+  static constexpr int kStages = D == 256 ? 2 : (D == 128 ? 6 : 11);
   // O buffers in tensor memory (after S_0, S_1): two let an item's epilogue
   // run while the next item accumulates into the other.
   static constexpr int kOBufs = D == 256 ? 1 : 2;
@@ -241,8 +258,8 @@ struct DCfg {
   static constexpr int kKVOff = kQOff + kQArea;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   // q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] pv_done
-  // o_full[2] o_empty[2] drain
-  static constexpr int kNumBars = 4 + 2 * kStages + 2 + 2 + 1 + 4 + 1;
+  // o_full[2] o_empty[2] drain epi
+  static constexpr int kNumBars = 4 + 2 * kStages + 2 + 2 + 1 + 4 + 1 + 1;
   // The CTA's item list, then the misc words.
   static constexpr int kItemOff = (kBarOff + kNumBars * 8 + 15) & ~15;
   static constexpr int kMiscOff = kItemOff + kMaxItems * static_cast<int>(sizeof(ItemRef)) + 16;
@@ -277,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_o_full = bar_pv_done + 8;                    // + 8 obuf
   const uint32_t bar_o_empty = bar_o_full + 16;                   // + 8 obuf
   const uint32_t bar_drain = bar_o_empty + 16;
+  const uint32_t bar_epi = bar_drain + 8;  // the softmax warps' epilogue stores are done
   ItemRef* items = reinterpret_cast<ItemRef*>(smem + C::kItemOff);
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
   // misc[0]: tensor-memory base address, misc[1]: abort flag, misc[2]: items
@@ -307,9 +325,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(bar_pv_done, 1);
     ptx::mbar_init(bar_drain, 1);
+    ptx::mbar_init(bar_epi, nact);
     misc[1] = 0;
-    misc[2] = static_cast<uint32_t>(build_items(p, items));
     ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    const int n = build_items(p, items, lane);
+    if (lane == 0) misc[2] = static_cast<uint32_t>(n);
   }
   // Rows R.. of each Q box are never loaded: zero them once so that the MMA
   // rows of the softmax warps' lanes past R read defined values (their
@@ -354,7 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ===================================================== TMA producer
     if (lane == 0) {
       const uint64_t pol_q = ptx::policy_evict_first();
-      const uint64_t pol_kv = ptx::policy_evict_first();  // the cache is streamed once
+      // A single position tile streams the cache once; several (prefill, or
+      // long query chunks) read each K/V tile again: keep those in L2.
+      const uint64_t pol_kv =
+          p.n_ptiles > 1 ? ptx::policy_evict_last() : ptx::policy_evict_first();
       uint32_t armed = 0, armed_parity = 0;  // per slot: loaded at least once / last parity
       int idx = 0, kw = 0;                   // ring entries, items with keys so far
       bool ok = true;
@@ -536,8 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // item's O buffer `ob` is final (its completion number ekw / kOBufs on
     // o_full[ob]). The tensor-memory loads are warp-collective (.sync.aligned):
     // every lane issues them; only real rows store.
-    auto split_epilogue = [&](bool valid, size_t prow, size_t lrow, float l_run, float m_use,
-                              int ekw) -> bool {
+    // Partial result of a piece: O / l (fp32) and its LSE to row `row` of
+    // slot `piece`, once the item's O buffer is final (its completion number
+    // ekw / kOBufs on o_full[ob]). The tensor-memory loads are warp-collective
+    // (.sync.aligned): every lane issues them; only real rows store.
+    auto split_epilogue = [&](bool valid, int piece, float l_run, float m_use, int ekw) -> bool {
       const int ob = ekw % C::kOBufs;
       const uint32_t tO = tmem + lane_base + kColO + static_cast<uint32_t>(ob * D);
       bool w = ptx::mbar_wait(bar_o_full + 8 * ob, static_cast<uint32_t>(ekw / C::kOBufs) & 1u,
@@ -548,9 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       }
       ptx::tc_fence_after();
+      const size_t prow = static_cast<size_t>(piece) * p.R + row;
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
       if (valid)
-        p.lse_part[lrow] = l_run > 0.f
+        p.lse_part[prow] = l_run > 0.f
                                ? ((m_use == -INFINITY ? 0.f : m_use) + __log2f(l_run)) * kLn2
                                : -INFINITY;
       float* dst = p.o_part + prow * D;
@@ -578,9 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // first P is stored, so that it runs while the tensor cores work.
     const bool defer = p.persistent > 0 && C::kOBufs == 2;
     bool pending = false, pend_valid = false;
-    size_t pend_prow = 0, pend_lrow = 0;
+    int pend_piece = 0, pend_kw = 0;
     float pend_l = 0.f, pend_m = 0.f;
-    int pend_kw = 0;
 
     int R = 0, kw = 0, ring = 0;  // S/PV steps, items with keys, ring entries so far
     bool ok = true;
@@ -699,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ptx::mbar_arrive(bar_p_full + 8 * buf);
         if (r == 0 && pending) {
           pending = false;
-          if (!split_epilogue(pend_valid, pend_prow, pend_lrow, pend_l, pend_m, pend_kw)) {
+          if (!split_epilogue(pend_valid, pend_piece, pend_l, pend_m, pend_kw)) {
             ok = false;
             break;
           }
@@ -709,18 +737,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- epilogue of the item
       if (p.persistent > 0) {
-        // Partial result: row `row` of slot I.piece.
-        const size_t prow = static_cast<size_t>(I.piece) * p.R + row;
-        const size_t lrow = prow;
         if (defer) {
           pending = true;
           pend_valid = valid;
-          pend_prow = prow;
-          pend_lrow = lrow;
+          pend_piece = I.piece;
           pend_l = l_run;
           pend_m = m_use;
           pend_kw = kw;
-        } else if (!split_epilogue(valid, prow, lrow, l_run, m_use, kw)) {
+        } else if (!split_epilogue(valid, I.piece, l_run, m_use, kw)) {
           ok = false;
           break;
         }
@@ -754,13 +778,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tile::stage_bf16_sw128(stage, kBoxBytes, row, c0, o, inv_l);
         }
         ptx::fence_proxy_async_smem();
-        ptx::named_bar_sync(1, 32 * nact);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_epi);
+        // Every softmax warp has staged its rows (bounded wait): store.
         if (warp == 0 && lane == 0) {
+          if (ptx::mbar_wait(bar_epi, 0, limit)) {
 #pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            ptx::tma_store_4d(&tm_o, sQ + bx * kBoxBytes, bx * 64, I.hk * p.G, I.sq0, I.b);
-          ptx::tma_store_commit();
-          ptx::tma_store_wait_read();
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              ptx::tma_store_4d(&tm_o, sQ + bx * kBoxBytes, bx * 64, I.hk * p.G, I.sq0, I.b);
+            ptx::tma_store_commit();
+            ptx::tma_store_wait_read();
+          } else {
+            fail();
+          }
         }
         if (valid && p.lse != nullptr)
           p.lse[(static_cast<size_t>(I.b) * p.H + h) * p.Sq + sq] =
@@ -773,8 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ring += 2 * n;
       }
     }
-    if (ok && pending)
-      split_epilogue(pend_valid, pend_prow, pend_lrow, pend_l, pend_m, pend_kw);
+    if (ok && pending) split_epilogue(pend_valid, pend_piece, pend_l, pend_m, pend_kw);
   }
 
   ptx::tc_fence_before();
