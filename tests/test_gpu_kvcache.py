@@ -120,6 +120,21 @@ def test_cache_rows_past_the_length_are_never_used(oracle_mod):
     _case(oracle_mod, 2, 1, 700, 8, 2, 64, [700, 5], False, -1, nan_tail=True, num_splits=3)
 
 
+def test_stream_k_quotas_spanning_many_sequences(oracle_mod):
+    """The automatic plan on 60 short sequences of one KV head (60 units,
+    fewer than half the SMs, 60 position-tile groups): CTA quotas of key tiles
+    cover pieces of several sequences, some with no keys (whose rows must come
+    out 0 / -inf), some cut at a quota boundary; NaN planted past every
+    length."""
+    rng = np.random.default_rng(61)
+    lens = [int(x) for x in rng.integers(0, 700, size=60)]
+    lens[3] = 0
+    lens[17] = 0
+    lens[40] = 699
+    _case(oracle_mod, 60, 1, 700, 4, 1, 128, lens, True, -1, nan_tail=True, seed=61)
+    _case(oracle_mod, 60, 2, 700, 8, 1, 64, lens, True, 100, seed=62)
+
+
 def test_full_caches_without_lengths(oracle_mod):
     _case(oracle_mod, 2, 3, 900, 8, 2, 128, [900, 900], True, -1, pass_lens=False)
 

@@ -91,6 +91,16 @@ def test_window_bounds_the_tiles_to_split():
     assert splits_none <= 65
 
 
+def test_more_groups_than_an_item_list_holds_take_fixed_splits():
+    # 100 batches x 1 KV head on a 400-SM device: 100 units, fewer than half
+    # the SMs, but 100 position-tile groups exceed the 80 items a CTA's list
+    # holds, so the plan falls back to even splits (about two CTAs per SM:
+    # ceil(800 / 100) = 8)
+    splits, ws = _plan(100, 1, 8192, 8, 1, 128, num_sms=400)
+    assert splits == _expected_splits(8, 64)
+    assert ws == _ws(100 * splits, 8)
+
+
 def test_position_tiles_count_as_units():
     # Sq = 64 with 4 heads per KV head: 2 position tiles of 32 positions
     # (R = 128 rows); Sq = 32: one.
