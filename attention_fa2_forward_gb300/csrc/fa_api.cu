@@ -306,6 +306,8 @@ fa_status_t check_forward_args(void* out, float* lse, const void* q, const void*
   return FA_OK;
 }
 
+fa_status_t current_sm_count(int* out);
+
 fa_status_t forward(void* out, float* lse, const void* q, const void* k, const void* v, int B,
                     int S, int H, int Hkv, int D, float scale, int mask_kind,
                     int local_window_size, int dtype, void* stream,
@@ -338,6 +340,7 @@ fa_status_t forward(void* out, float* lse, const void* q, const void* k, const v
   p.status = status;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.stall_probe = g_stall_probe.load();
+  if ((st = current_sm_count(&p.num_sms)) != FA_OK) return st;
   if (FA_TRACE) {
     p.trace = g_trace_buf.load();
     p.trace_ctas = p.trace != nullptr

@@ -94,7 +94,8 @@ struct Cfg {
   static constexpr int kKVOff = kQOff + QT * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   // q_full[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] drain
-  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1;
+  // q_free[2] (persistent kernel)
+  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColO = 128 * QT;              // O_t at kColO + t * D
@@ -549,6 +550,544 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
   }
 }
 
+// ---------------------------------------------------------------- persistent
+// The same work as fa_fwd_bf16_tc_kernel with persistent CTAs, one per
+// resident slot, each walking a sequence of items (query blocks): the ring,
+// the S/P phases and the O phases carry on from one item to the next, and a
+// tile's next Q loads as soon as the store of its previous O has read the Q
+// buffer it was staged over. Used for one-tile CTAs when the items outnumber
+// the resident slots (short sequences: their items are a few KV steps, and
+// per-CTA set-up and epilogue would otherwise be a large share). The
+// single-item kernel above stays separate: the item loop, compiled into it,
+// made its steps ~2-4 % slower.
+// One work item: the QT Q tiles of query block qb of head h, batch b (the
+// heaviest -- last -- query blocks first), and the KV tile range [lo_t, hi_t)
+// of each tile; empty when the tile is past S (and for tile 1 of a one-tile
+// CTA).
+struct QItem {
+  int b, h, hk, qb;
+  int q0[kMaxQTiles], lo[kMaxQTiles], hi[kMaxQTiles];
+  int jlo, jhi;
+};
+
+template <int QT>
+__device__ __forceinline__ QItem decode_qitem(const FwdProblem& p, int item, int num_qblocks) {
+  QItem w;
+  const int per_qb = p.H * p.B;
+  w.qb = num_qblocks - 1 - item / per_qb;
+  const int rem = item % per_qb;
+  w.h = rem % p.H;
+  w.b = rem / p.H;
+  w.hk = w.h / (p.H / p.Hkv);
+#pragma unroll
+  for (int t = 0; t < kMaxQTiles; ++t) {
+    w.q0[t] = w.qb * (QT * kBM) + t * kBM;
+    if (t < QT && w.q0[t] < p.S) {
+      // Window without the causal mask: keys up to the last row + W - 1.
+      const int kv_end = p.causal ? min(p.S, w.q0[t] + kBM)
+                                  : (p.window > 0 ? min(p.S, w.q0[t] + kBM - 1 + p.window) : p.S);
+      const int kv_begin = p.window > 0 ? max(0, w.q0[t] - p.window + 1) : 0;
+      w.lo[t] = kv_begin / kBN;
+      w.hi[t] = (kv_end + kBN - 1) / kBN;
+    } else {
+      w.lo[t] = w.hi[t] = 0;
+    }
+  }
+  w.jlo = w.lo[0];
+  w.jhi = max(w.hi[0], w.hi[1]);
+  return w;
+}
+
+// Persistent schedule: item number of this CTA's k-th item, or -1. The CTAs
+// take the items in rounds, snake order: round r gives CTA g item r * C + g
+// for even r and r * C + C - 1 - g for odd r, so the heavy items of one round
+// and the light ones of the next pair up.
+__device__ __forceinline__ int qitem_at(int k, int n_items) {
+  const int C = static_cast<int>(gridDim.x);
+  const int pos = (k & 1) ? C - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  const long long it = static_cast<long long>(k) * C + pos;
+  return it < n_items ? static_cast<int>(it) : -1;
+}
+
+template <int D, int QT>
+__global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
+    fa_fwd_bf16_tc_persistent_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_o, const FwdProblem p,
+                          int num_qblocks) {
+  using C = Cfg<D, QT>;
+  constexpr int kSoftmaxWarps = Roles<QT>::kSoftmaxWarps;
+  constexpr int kMmaWarp = Roles<QT>::kMmaWarp;
+  constexpr int kLoadWarp = Roles<QT>::kLoadWarp;
+  constexpr uint32_t kTmemCols = Roles<QT>::kTmemCols;
+  (void)kSoftmaxWarps;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+
+  const uint32_t sQ = base + C::kQOff;
+  const uint32_t sKV = base + C::kKVOff;
+  const uint32_t bars = base + C::kBarOff;
+  const uint32_t bar_q_full = bars;                              // + 8 t
+  const uint32_t bar_kv_full = bars + 8 * 2;                     // + 8 s
+  const uint32_t bar_kv_empty = bars + 8 * (2 + C::kStages);     // + 8 s
+  const uint32_t bar_s_full = bars + 8 * (2 + 2 * C::kStages);   // + 8 t
+  const uint32_t bar_p_full = bar_s_full + 16;                   // + 8 t
+  const uint32_t bar_o_full = bar_p_full + 16;                   // + 8 t
+  const uint32_t bar_drain = bar_o_full + 16;
+  const uint32_t bar_q_free = bar_drain + 8;  // + 8 t: tile t's O stored, its Q buffer free
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
+  // misc[0]: tensor-memory base address, misc[1]: abort flag, misc[2 + t]:
+  // tile t's softmax warps stop
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  namespace tr = trace;
+  const int trace_role = warp == kLoadWarp ? tr::kRoleProducer
+                         : warp == kMmaWarp ? tr::kRoleMma
+                                            : tr::softmax_role(warp);
+  tr::Recorder rec(p.trace, p.trace_ctas, trace_role, lane == 0);
+  if (warp == kLoadWarp) rec(tr::kCtaStart, tr::sm_id());
+
+  const int n_items = num_qblocks * p.H * p.B;
+  const unsigned long long limit = p.wait_limit_ns;
+  const unsigned long long drain_limit = limit + kDrainExtraNs;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int t = 0; t < kMaxQTiles; ++t) {
+      ptx::mbar_init(bar_q_full + 8 * t, 1);
+      ptx::mbar_init(bar_s_full + 8 * t, 1);
+      ptx::mbar_init(bar_p_full + 8 * t, 4);  // one arrival per softmax warp
+      ptx::mbar_init(bar_o_full + 8 * t, 1);
+      ptx::mbar_init(bar_q_free + 8 * t, 1);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(bar_kv_full + 8 * s, 1);
+      ptx::mbar_init(bar_kv_empty + 8 * s, 1);
+    }
+    ptx::mbar_init(bar_drain, 1);
+    misc[1] = 0;
+    misc[2] = misc[3] = 0;  // per tile: a softmax warp timed out
+    ptx::fence_mbar_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    ptx::tma_prefetch_desc(&tm_q);
+    ptx::tma_prefetch_desc(&tm_k);
+    ptx::tma_prefetch_desc(&tm_v);
+    ptx::tma_prefetch_desc(&tm_o);
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(base + C::kMiscOff, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  auto fail = [&]() {
+    misc[1] = 1;
+    atomicOr(p.status, kStatusWaitTimeout);
+  };
+  auto aborted = [&]() { return misc[1] != 0; };
+
+  if (warp == kLoadWarp) {
+    // ===================================================== TMA producer
+    if (lane == 0) {
+      const uint64_t pol_q = ptx::policy_evict_first();
+      const uint64_t pol_kv = ptx::policy_evict_last();
+      uint32_t armed = 0, armed_parity = 0;  // per slot: bit set once loaded / last parity
+      int idx = 0;                           // ring entries so far
+      int nq[kMaxQTiles] = {0, 0};           // Q loads per tile so far
+      bool ok = true;
+      for (int k = 0, item; ok && (item = qitem_at(k, n_items)) >= 0; ++k) {
+        const QItem w = decode_qitem<QT>(p, item, num_qblocks);
+#pragma unroll
+        for (int t = 0; t < QT; ++t) {
+          if (!ok || w.lo[t] >= w.hi[t]) continue;
+          // The previous item's O of this tile was staged over its Q
+          // buffer: load the next Q once that store has read it.
+          if (nq[t] > 0 &&
+              (aborted() || !ptx::mbar_wait(bar_q_free + 8 * t,
+                                            static_cast<uint32_t>(nq[t] - 1) & 1u, limit))) {
+            fail();
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(bar_q_full + 8 * t, C::kTileBytes);
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            ptx::tma_load_4d(sQ + t * C::kTileBytes + bx * C::kBoxBytes, &tm_q, bar_q_full + 8 * t,
+                             bx * C::kBoxCols, w.h, w.q0[t], w.b, pol_q);
+          ++nq[t];
+          rec(tr::kQLoadIssued, t);
+        }
+        // Ring order: K_jlo, V_jlo, K_jlo+1, V_jlo+1, ...
+        for (int j = w.jlo; j < w.jhi && ok; ++j) {
+          for (int kind = 0; kind < 2; ++kind, ++idx) {
+            const int s = idx % C::kStages;
+            const uint32_t ph = static_cast<uint32_t>(idx / C::kStages) & 1u;
+            if (aborted() || !ptx::mbar_wait(bar_kv_empty + 8 * s, ph ^ 1u, limit)) {
+              fail();
+              ok = false;
+              break;
+            }
+            // A tile starting past the last key would be a planning error.
+            tr::guard(j * kBN < p.S, p.status, kStatusBoundsGuard);
+            ptx::mbar_arrive_expect_tx(bar_kv_full + 8 * s, C::kTileBytes);
+            const CUtensorMap* tm = kind == 0 ? &tm_k : &tm_v;
+#pragma unroll
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              ptx::tma_load_4d(sKV + s * C::kTileBytes + bx * C::kBoxBytes, tm,
+                               bar_kv_full + 8 * s, bx * C::kBoxCols, w.hk, j * kBN, w.b, pol_kv);
+            rec(kind == 0 ? tr::kKLoadIssued : tr::kVLoadIssued, j);
+            armed |= 1u << s;
+            armed_parity = (armed_parity & ~(1u << s)) | (ph << s);
+          }
+        }
+      }
+      // Never leave while a copy of ours may still be writing shared memory.
+#pragma unroll
+      for (int t = 0; t < QT; ++t)
+        if (nq[t] > 0)
+          ptx::mbar_wait(bar_q_full + 8 * t, static_cast<uint32_t>(nq[t] - 1) & 1u, drain_limit);
+      for (int s = 0; s < C::kStages; ++s)
+        if ((armed >> s) & 1u) ptx::mbar_wait(bar_kv_full + 8 * s, (armed_parity >> s) & 1u, drain_limit);
+    }
+  } else if (warp == kMmaWarp) {
+    // ===================================================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBM, D, false, true);
+      bool ok = true;
+      // Test hook: wait on the drain barrier, which nothing signals before
+      // this thread's own final commit, so the bounded wait must expire.
+      if (p.stall_probe && !ptx::mbar_wait(bar_drain, 0, limit)) {
+        fail();
+        ok = false;
+      }
+      // The current item's KV ranges (updated per item; the lambdas read them).
+      int lo[kMaxQTiles] = {0, 0}, hi[kMaxQTiles] = {0, 0};
+      auto in_tile = [&](int t, int j) { return j >= lo[t] && j < hi[t]; };
+      // Wait for ring entry idx; returns its slot or -1 on time-out.
+      auto wait_kv = [&](int idx) -> int {
+        const int s = idx % C::kStages;
+        const uint32_t ph = static_cast<uint32_t>(idx / C::kStages) & 1u;
+        if (aborted() || !ptx::mbar_wait(bar_kv_full + 8 * s, ph, limit)) {
+          fail();
+          return -1;
+        }
+        ptx::tc_fence_after();
+        return s;
+      };
+      // K-major Q and K: 8-row groups 8 box rows apart. MN-major V: atoms
+      // of kBoxCols columns one box apart.
+      const uint64_t dq0 = ptx::smem_desc(sQ, 16, 8 * C::kRowBytes, C::kSwizzle);
+      const uint64_t dk0 = ptx::smem_desc(sKV, 16, 8 * C::kRowBytes, C::kSwizzle);
+      const uint64_t dv0 = ptx::smem_desc(sKV, C::kBoxBytes, 8 * C::kRowBytes, C::kSwizzle);
+      auto issue_s = [&](int t, int kslot, int j) {
+        const uint64_t dq = dq0 + static_cast<uint32_t>((t * C::kTileBytes) >> 4);
+        const uint64_t dk = dk0 + static_cast<uint32_t>((kslot * C::kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = static_cast<uint32_t>(
+              ((kk / C::kKPerBox) * C::kBoxBytes + (kk % C::kKPerBox) * 32) >> 4);
+          ptx::mma_ss(tmem + t * kBN, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        ptx::tc_commit(bar_s_full + 8 * t);
+        rec(tr::kSIssued, (t << 16) | j);
+      };
+      auto issue_pv = [&](int t, int vslot, bool accumulate, int j) {
+        const uint64_t dv = dv0 + static_cast<uint32_t>((vslot * C::kTileBytes) >> 4);
+        const uint32_t acc = accumulate ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          ptx::mma_ts(tmem + C::kColO + t * D, tmem + t * kBN + kk * 8,
+                      dv + static_cast<uint32_t>(kk * (16 * C::kRowBytes >> 4)), kIdescPV,
+                      kk > 0 ? 1u : acc);
+        rec(tr::kPvIssued, (t << 16) | j);
+      };
+      uint32_t p_phase[kMaxQTiles] = {0u, 0u};
+      auto wait_p = [&](int t, int j) -> bool {
+        if (aborted() || !ptx::mbar_wait(bar_p_full + 8 * t, p_phase[t], limit)) {
+          fail();
+          return false;
+        }
+        p_phase[t] ^= 1u;
+        ptx::tc_fence_after();
+        rec(tr::kPSeen, (t << 16) | j);
+        return true;
+      };
+
+      int base_idx = 0;             // ring entries of the items before this one
+      int nq[kMaxQTiles] = {0, 0};  // Q loads per tile seen so far
+      for (int k = 0, item; ok && (item = qitem_at(k, n_items)) >= 0; ++k) {
+        const QItem w = decode_qitem<QT>(p, item, num_qblocks);
+#pragma unroll
+        for (int t = 0; t < kMaxQTiles; ++t) {
+          lo[t] = w.lo[t];
+          hi[t] = w.hi[t];
+        }
+        const int jlo = w.jlo, jhi = w.jhi;
+#pragma unroll
+        for (int t = 0; t < QT; ++t) {
+          if (ok && lo[t] < hi[t]) {
+            if (!ptx::mbar_wait(bar_q_full + 8 * t, static_cast<uint32_t>(nq[t]) & 1u, limit)) {
+              fail();
+              ok = false;
+            }
+            ++nq[t];
+          }
+        }
+        if (!ok) break;
+        rec(tr::kQReady, 0);
+        {
+          const int ks = wait_kv(base_idx);
+          if (ks < 0) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int t = 0; t < QT; ++t)
+            if (in_tile(t, jlo)) issue_s(t, ks, jlo);
+          ptx::tc_commit(bar_kv_empty + 8 * ks);
+        }
+        for (int j = jlo; ok && j < jhi; ++j) {
+          const int rel = j - jlo;
+          const int vs = wait_kv(base_idx + 2 * rel + 1);
+          if (vs < 0) {
+            ok = false;
+            break;
+          }
+          if (in_tile(0, j)) {
+            if (!wait_p(0, j)) {
+              ok = false;
+              break;
+            }
+            issue_pv(0, vs, j > lo[0], j);
+            if (j == hi[0] - 1) ptx::tc_commit(bar_o_full);
+          }
+          const bool has_next = j + 1 < jhi;
+          int ks = -1;
+          if (has_next) {
+            ks = wait_kv(base_idx + 2 * rel + 2);
+            if (ks < 0) {
+              ok = false;
+              break;
+            }
+            if (in_tile(0, j + 1)) issue_s(0, ks, j + 1);
+          }
+          if (QT > 1 && in_tile(1, j)) {
+            if (!wait_p(1, j)) {
+              ok = false;
+              break;
+            }
+            issue_pv(1, vs, j > lo[1], j);
+            if (j == hi[1] - 1) ptx::tc_commit(bar_o_full + 8);
+          }
+          ptx::tc_commit(bar_kv_empty + 8 * vs);
+          if (has_next) {
+            if (QT > 1 && in_tile(1, j + 1)) issue_s(1, ks, j + 1);
+            ptx::tc_commit(bar_kv_empty + 8 * ks);
+          }
+        }
+        base_idx += 2 * (jhi - jlo);
+      }
+      // Every MMA must have finished before tensor memory is released.
+      ptx::tc_commit(bar_drain);
+      ptx::mbar_wait(bar_drain, 0, drain_limit);
+      rec(tr::kMmaDrained, 0);
+    }
+    __syncwarp();
+  } else {
+    // ===================================================== softmax warpgroups
+    const int t = warp >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * kBN;
+    const uint32_t tO = tmem + lane_base + C::kColO + t * D;
+    const float c = p.scale_log2;
+    // A zero scale makes every visible score 0: use 0 as the score and 1 as
+    // the multiplier.
+    const bool zero_scale = !(c > 0.f);
+    const float ce = zero_scale ? 1.f : c;
+
+    bool ok = true;
+    uint32_t s_phase = 0;  // parity of the S(t) MMAs seen so far
+    int nw = 0;            // items with work for this tile so far
+    for (int k = 0; ok; ++k) {
+      const int item = qitem_at(k, n_items);
+      if (item < 0) break;
+      const QItem w = decode_qitem<QT>(p, item, num_qblocks);
+      // This warpgroup's tile, selected without run-time array indexing.
+      const int tq0 = t == 0 ? w.q0[0] : w.q0[1];
+      const int tlo = t == 0 ? w.lo[0] : w.lo[1];
+      const int thi = t == 0 ? w.hi[0] : w.hi[1];
+      if (tlo >= thi) continue;
+      const int i = tq0 + row;
+      const RowBounds rb = row_bounds(p, i);
+
+      float m_use = -INFINITY;  // running max of score * scale * log2(e) (possibly stale)
+      float l_run = 0.f;        // running sum of 2^(x - m_use)
+      for (int j = tlo; j < thi; ++j) {
+        bool wv = ptx::mbar_wait(bar_s_full + 8 * t, s_phase, limit);
+        s_phase ^= 1u;
+        wv = __all_sync(0xffffffffu, wv);
+        if (!wv) {
+          fail();
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        rec(tr::kSReady, j);
+
+        uint32_t r[kBN];
+#pragma unroll
+        for (int c0 = 0; c0 < kBN; c0 += 32) ptx::tmem_ld_32x32b_x32(tS + c0, r + c0);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<kBN>(r);
+        rec(tr::kSLoaded, j);
+
+        const int k0 = j * kBN;
+        bool full = k0 + kBN <= p.S;
+        if (p.causal) full = full && (k0 + kBN - 1 <= tq0);
+        if (p.window > 0) full = full && (tq0 + kBM - 1 - k0 < p.window);
+        if (p.window > 0 && !p.causal) full = full && (k0 + kBN - 1 - tq0 < p.window);
+        const int vlo = rb.lo == INT_MIN ? INT_MIN : rb.lo - k0;
+        const int vhi = rb.hi - k0;
+
+        // Tiles that straddle the mask boundary (or a zero scale): hide the
+        // invisible scores in place, then every tile takes the same path.
+        if (!full || zero_scale) tile::mask_cols(r, vlo, vhi, zero_scale);
+
+        // Row maximum of the (visible) scores.
+        const float mx = tile::row_max(r);
+        if (FA_TRACE) {
+          asm volatile("" ::"f"(mx));
+          rec(tr::kMaxDone, j);
+        }
+        const float m_tile = mx == -INFINITY ? -INFINITY : mx * ce;
+        const float m_new = fmaxf(m_use, m_tile);
+        const bool first = j == tlo;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (first) {
+          m_use = m_new;
+        } else if (m_new > m_use + kRescaleThreshold) {
+          alpha = ptx::ex2_approx(m_use - m_new);  // m_use may be -inf: alpha = 0
+          m_use = m_new;
+          rescale = true;
+        }
+        const float neg_base = m_use == -INFINITY ? 0.f : -m_use;
+
+        // P = 2^(x - m_use) (hidden scores are -inf and give 0) as bf16 pairs
+        // written over S, and the row sum.
+        const float row_sum = tile::exp2_to_bf16(r, ce, neg_base);
+        l_run = l_run * alpha + row_sum;
+        if (FA_TRACE) {
+          asm volatile("" ::"f"(l_run), "r"(r[0]), "r"(r[63]));
+          rec(tr::kExpDone, j);
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < kBN / 2; c0 += 32) ptx::tmem_st_32x32b_x32(tS + c0, r + c0);
+
+        // Lazy correction of the O accumulator (previous PV has completed:
+        // the S MMA this iteration waited for was issued after it).
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            ptx::tmem_ld_32x32b_x32(tO + c0, o);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st_32x32b_x32(tO + c0, o);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_p_full + 8 * t);
+        rec(tr::kPReady, j | (rescale ? 1u << 23 : 0u));
+      }
+
+      // ---- epilogue: O / l -> bf16 -> shared (swizzled, over this tile's Q
+      // buffer: its S MMAs are done) -> TMA store; LSE. A warp that timed out
+      // records it in misc[2 + t] before the tile's barrier, so the four warps
+      // leave together.
+      if (ok) {
+        bool wv = ptx::mbar_wait(bar_o_full + 8 * t, static_cast<uint32_t>(nw) & 1u, limit);
+        wv = __all_sync(0xffffffffu, wv);
+        if (!wv) {
+          fail();
+          ok = false;
+        }
+      }
+      if (!ok && lane == 0) misc[2 + t] = 1;
+      // A store of rows that start past S would be a planning error.
+      const bool do_store = ok && tr::guard(tq0 < p.S, p.status, kStatusBoundsGuard);
+      if (do_store) {
+        rec(tr::kEpilogueStart, 0);
+        ptx::tc_fence_after();
+        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+        uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          ptx::tmem_ld_32x32b_x32(tO + c0, o);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence<32>(o);
+          if (D == 96)
+            tile::stage_bf16_sw64(stage, C::kBoxBytes, row, c0, o, inv_l);
+          else
+            tile::stage_bf16_sw128(stage, C::kBoxBytes, row, c0, o, inv_l);
+        }
+        ptx::fence_proxy_async_smem();
+      }
+      ptx::named_bar_sync(1 + t, 128);
+      const bool failed = misc[2 + t] != 0;
+      if (quad == 0 && lane == 0) {
+        if (!failed && do_store) {
+#pragma unroll
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            ptx::tma_store_4d(&tm_o, sQ + t * C::kTileBytes + bx * C::kBoxBytes,
+                              bx * C::kBoxCols, w.h, tq0, w.b);
+          ptx::tma_store_commit();
+          ptx::tma_store_wait_read();
+        }
+        // This tile's Q buffer may take the next item's Q.
+        ptx::mbar_arrive(bar_q_free + 8 * t);
+      }
+      if (failed) {
+        ok = false;
+        break;
+      }
+      if (do_store && p.lse != nullptr && i < p.S) {
+        const float m_fin = m_use == -INFINITY ? 0.f : m_use;
+        const long long idx = (static_cast<long long>(w.b) * p.H + w.h) * p.S + i;
+        const long long lse_limit =
+            p.lse_limit > 0 ? p.lse_limit : static_cast<long long>(p.B) * p.H * p.S;
+        if (tr::guard(idx < lse_limit, p.status, kStatusBoundsGuard))
+          p.lse[idx] = (m_fin + __log2f(l_run)) * kLn2;
+      }
+      if (do_store) rec(tr::kEpilogueEnd, 0);
+      ++nw;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 template <int D, int QT>
 cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* k, const void* v,
                      cudaStream_t stream) {
@@ -566,6 +1105,22 @@ cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* 
   const int nqb = (p.S + QT * kBM - 1) / (QT * kBM);
   const long long grid = static_cast<long long>(nqb) * p.H * p.B;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+  // One-tile CTAs, more items than resident slots: the persistent kernel
+  // (not in the debug build, whose trace records one item per CTA).
+  if constexpr (QT == 1 && !FA_TRACE) {
+    const long long slots = static_cast<long long>(p.num_sms) * Roles<QT>::kCtasPerSm;
+    if (p.num_sms > 0 && grid > slots) {
+      static unsigned long long attr_done = 0;
+      cudaError_t err = ensure_smem_attr(&attr_done, reinterpret_cast<const void*>(
+                                                         &fa_fwd_bf16_tc_persistent_kernel<D, QT>),
+                                         C::kSmemBytes);
+      if (err != cudaSuccess) return err;
+      fa_fwd_bf16_tc_persistent_kernel<D, QT>
+          <<<static_cast<unsigned>(slots), Roles<QT>::kThreads, C::kSmemBytes, stream>>>(
+              tq, tk, tv, to, p, nqb);
+      return cudaGetLastError();
+    }
+  }
   static unsigned long long attr_done = 0;
   cudaError_t err = ensure_smem_attr(&attr_done, reinterpret_cast<const void*>(
                                                      &fa_fwd_bf16_tc_kernel<D, QT>),

@@ -45,6 +45,7 @@ struct FwdProblem {
   long long trace_ctas = 0;    // CTAs the trace buffer has room for
   long long lse_limit = 0;     // debug build: LSE elements a guard lets the kernel write
   bool cache_maps = true;      // false: encode the tensor maps without the (allocating) cache
+  int num_sms = 0;             // > 0: the device's SMs; the bf16 kernel may then run persistent
 };
 
 // Attention over a KV cache (bf16, tensor cores): batch b holds L_b keys at

@@ -90,6 +90,20 @@ def test_mha_s1024_d64_workload_whole(oracle_mod):
     _compare(out, lse, ref_out, ref_lse, torch.bfloat16, w.name)
 
 
+@pytest.mark.parametrize("B,S,H,Hkv,D,causal,window", [
+    (4, 1000, 24, 8, 64, True, -1),    # GQA, ragged last tile
+    (4, 1000, 24, 8, 64, True, 200),   # causal window
+    (3, 1024, 32, 32, 40, False, -1),  # no mask, padded head dim
+    (2, 777, 48, 4, 64, False, 90),    # two-sided window, ragged
+])
+def test_persistent_short_sequence_schedule(oracle_mod, B, S, H, Hkv, D, causal, window):
+    """Head dims up to 64 on sequences up to 1024 with more query tiles than
+    the GPU holds CTAs at once (here 400 to 768): persistent CTAs walk the
+    tiles, each tile's Q loading while the previous tile finishes; every
+    element and LSE row is checked."""
+    _full_case(oracle_mod, B, S, H, Hkv, D, torch.bfloat16, causal, window, seed=900 + S + H)
+
+
 # --- the long workloads at full size, every element ----------------------------------
 
 def _sample_rows(S, seed, n_random=40):
