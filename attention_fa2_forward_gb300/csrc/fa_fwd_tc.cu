@@ -94,8 +94,7 @@ struct Cfg {
   static constexpr int kKVOff = kQOff + QT * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   // q_full[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_full[2] drain
-  // q_free[2] (persistent kernel)
-  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1 + 2;
+  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColO = 128 * QT;              // O_t at kColO + t * D
@@ -551,50 +550,81 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
 }
 
 // ---------------------------------------------------------------- persistent
-// The same work as fa_fwd_bf16_tc_kernel with persistent CTAs, one per
-// resident slot, each walking a sequence of items (query blocks): the ring,
-// the S/P phases and the O phases carry on from one item to the next, and a
-// tile's next Q loads as soon as the store of its previous O has read the Q
-// buffer it was staged over. Used for one-tile CTAs when the items outnumber
-// the resident slots (short sequences: their items are a few KV steps, and
-// per-CTA set-up and epilogue would otherwise be a large share). The
-// single-item kernel above stays separate: the item loop, compiled into it,
-// made its steps ~2-4 % slower.
-// One work item: the QT Q tiles of query block qb of head h, batch b (the
-// heaviest -- last -- query blocks first), and the KV tile range [lo_t, hi_t)
-// of each tile; empty when the tile is past S (and for tile 1 of a one-tile
-// CTA).
-struct QItem {
-  int b, h, hk, qb;
-  int q0[kMaxQTiles], lo[kMaxQTiles], hi[kMaxQTiles];
-  int jlo, jhi;
+// One Q tile per CTA (head dims up to 64), persistent CTAs, one per resident
+// slot, each walking a sequence of items (query blocks). With one tile of at
+// most 64 columns, 64 of the CTA's 256 tensor-memory columns are left over
+// after S (128) and O (64): P gets them to itself, so S(j+1) no longer waits
+// for PV(j) to have read P(j) out of S's columns. The MMA thread issues
+// S(j+1) as soon as the softmax has loaded S(j) into registers, and the
+// tensor core computes it while the softmax of step j runs; the softmax then
+// waits for PV(j-1) only before it overwrites P (and before a rescale of O).
+// Q is double-buffered, so the next item's Q is loaded during the current
+// item, and the first S of an item is computed during the previous item's
+// epilogue; the epilogue hands O back to the MMA thread (o_free) as soon as
+// it has read it out of tensor memory. The ring, the phases and the counts
+// carry on from one item to the next. Used for one-tile CTAs when the items
+// outnumber the resident slots (short sequences, whose items are a few KV
+// steps each).
+//
+// TMEM columns: S [0, 128), O [128, 128 + D), P [128 + D, 128 + D + 64).
+template <int D>
+struct PCfg {
+  static_assert(D == 64, "the persistent one-tile kernel is built for the 64-column layout");
+  using Geo = Cfg<D, 1>;  // TMA box geometry of the 64-column tiles
+  static constexpr int kBoxCols = Geo::kBoxCols;
+  static constexpr int kRowBytes = Geo::kRowBytes;
+  static constexpr int kBoxBytes = Geo::kBoxBytes;
+  static constexpr int kBoxes = Geo::kBoxes;
+  static constexpr int kKPerBox = Geo::kKPerBox;
+  static constexpr uint32_t kSwizzle = Geo::kSwizzle;
+  static constexpr int kTileBytes = Geo::kTileBytes;
+  static constexpr int kQBufs = 2;
+  static constexpr int kStages = 4;
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = kQOff + kQBufs * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  // q_full[2] q_free[2] kv_full[S] kv_empty[S] s_full s_free p_full pv_done
+  // o_full o_free drain
+  static constexpr int kNumBars = 2 * kQBufs + 2 * kStages + 7;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + slack for 1 KB alignment
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColO = kBN;
+  static constexpr uint32_t kColP = kBN + D;
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr int kThreads = 6 * 32;  // 4 softmax warps, MMA warp, TMA warp
+  static constexpr int kMmaWarp = 4;
+  static constexpr int kLoadWarp = 5;
+  static constexpr int kCtasPerSm = 2;
+  static_assert(kColP + kBN / 2 <= kTmemCols, "tensor memory");
+  static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024, "shared memory");
 };
 
-template <int QT>
+// One work item: the Q tile of query block qb of head h, batch b (the
+// heaviest -- last -- query blocks first), and its KV tile range [lo, hi).
+struct QItem {
+  int b, h, hk, q0, lo, hi;
+};
+
 __device__ __forceinline__ QItem decode_qitem(const FwdProblem& p, int item, int num_qblocks) {
   QItem w;
   const int per_qb = p.H * p.B;
-  w.qb = num_qblocks - 1 - item / per_qb;
+  const int qb = num_qblocks - 1 - item / per_qb;
   const int rem = item % per_qb;
   w.h = rem % p.H;
   w.b = rem / p.H;
   w.hk = w.h / (p.H / p.Hkv);
-#pragma unroll
-  for (int t = 0; t < kMaxQTiles; ++t) {
-    w.q0[t] = w.qb * (QT * kBM) + t * kBM;
-    if (t < QT && w.q0[t] < p.S) {
-      // Window without the causal mask: keys up to the last row + W - 1.
-      const int kv_end = p.causal ? min(p.S, w.q0[t] + kBM)
-                                  : (p.window > 0 ? min(p.S, w.q0[t] + kBM - 1 + p.window) : p.S);
-      const int kv_begin = p.window > 0 ? max(0, w.q0[t] - p.window + 1) : 0;
-      w.lo[t] = kv_begin / kBN;
-      w.hi[t] = (kv_end + kBN - 1) / kBN;
-    } else {
-      w.lo[t] = w.hi[t] = 0;
-    }
+  w.q0 = qb * kBM;
+  if (w.q0 < p.S) {
+    // Window without the causal mask: keys up to the last row + W - 1.
+    const int kv_end = p.causal ? min(p.S, w.q0 + kBM)
+                                : (p.window > 0 ? min(p.S, w.q0 + kBM - 1 + p.window) : p.S);
+    const int kv_begin = p.window > 0 ? max(0, w.q0 - p.window + 1) : 0;
+    w.lo = kv_begin / kBN;
+    w.hi = (kv_end + kBN - 1) / kBN;
+  } else {
+    w.lo = w.hi = 0;
   }
-  w.jlo = w.lo[0];
-  w.jhi = max(w.hi[0], w.hi[1]);
   return w;
 }
 
@@ -609,19 +639,41 @@ __device__ __forceinline__ int qitem_at(int k, int n_items) {
   return it < n_items ? static_cast<int>(it) : -1;
 }
 
-template <int D, int QT>
-__global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
+// Walks this CTA's KV steps in order, across its items (items with no KV
+// tile are skipped). u counts the items with work (their Q buffer is u & 1).
+struct StepCursor {
+  int k = -1, u = -1, j = 0;
+  QItem w;
+  bool valid = false;
+  __device__ __forceinline__ void next_item(const FwdProblem& p, int n_items, int nqb) {
+    for (;;) {
+      const int item = qitem_at(++k, n_items);
+      if (item < 0) {
+        valid = false;
+        return;
+      }
+      w = decode_qitem(p, item, nqb);
+      if (w.lo < w.hi) break;
+    }
+    ++u;
+    j = w.lo;
+    valid = true;
+  }
+  __device__ __forceinline__ void advance(const FwdProblem& p, int n_items, int nqb) {
+    if (++j >= w.hi) next_item(p, n_items, nqb);
+  }
+  __device__ __forceinline__ bool first() const { return j == w.lo; }
+  __device__ __forceinline__ bool last() const { return j == w.hi - 1; }
+};
+
+template <int D>
+__global__ void __launch_bounds__(PCfg<D>::kThreads, PCfg<D>::kCtasPerSm)
     fa_fwd_bf16_tc_persistent_kernel(const __grid_constant__ CUtensorMap tm_q,
-                          const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v,
-                          const __grid_constant__ CUtensorMap tm_o, const FwdProblem p,
-                          int num_qblocks) {
-  using C = Cfg<D, QT>;
-  constexpr int kSoftmaxWarps = Roles<QT>::kSoftmaxWarps;
-  constexpr int kMmaWarp = Roles<QT>::kMmaWarp;
-  constexpr int kLoadWarp = Roles<QT>::kLoadWarp;
-  constexpr uint32_t kTmemCols = Roles<QT>::kTmemCols;
-  (void)kSoftmaxWarps;
+                                     const __grid_constant__ CUtensorMap tm_k,
+                                     const __grid_constant__ CUtensorMap tm_v,
+                                     const __grid_constant__ CUtensorMap tm_o, const FwdProblem p,
+                                     int num_qblocks) {
+  using C = PCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -630,57 +682,62 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
   const uint32_t sQ = base + C::kQOff;
   const uint32_t sKV = base + C::kKVOff;
   const uint32_t bars = base + C::kBarOff;
-  const uint32_t bar_q_full = bars;                              // + 8 t
-  const uint32_t bar_kv_full = bars + 8 * 2;                     // + 8 s
-  const uint32_t bar_kv_empty = bars + 8 * (2 + C::kStages);     // + 8 s
-  const uint32_t bar_s_full = bars + 8 * (2 + 2 * C::kStages);   // + 8 t
-  const uint32_t bar_p_full = bar_s_full + 16;                   // + 8 t
-  const uint32_t bar_o_full = bar_p_full + 16;                   // + 8 t
-  const uint32_t bar_drain = bar_o_full + 16;
-  const uint32_t bar_q_free = bar_drain + 8;  // + 8 t: tile t's O stored, its Q buffer free
+  const uint32_t bar_q_full = bars;                             // + 8 buffer
+  const uint32_t bar_q_free = bars + 8 * C::kQBufs;             // + 8 buffer
+  const uint32_t bar_kv_full = bars + 16 * C::kQBufs;           // + 8 s
+  const uint32_t bar_kv_empty = bar_kv_full + 8 * C::kStages;   // + 8 s
+  const uint32_t bar_s_full = bar_kv_empty + 8 * C::kStages;    // S(n) in tensor memory
+  const uint32_t bar_s_free = bar_s_full + 8;                   // S(n) read by the softmax
+  const uint32_t bar_p_full = bar_s_free + 8;                   // P(n) stored, O corrected
+  const uint32_t bar_pv_done = bar_p_full + 8;                  // PV(n) completed
+  const uint32_t bar_o_full = bar_pv_done + 8;                  // item's last PV completed
+  const uint32_t bar_o_free = bar_o_full + 8;                   // item's O read out
+  const uint32_t bar_drain = bar_o_free + 8;
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
-  // misc[0]: tensor-memory base address, misc[1]: abort flag, misc[2 + t]:
-  // tile t's softmax warps stop
+  // misc[0]: tensor-memory base address, misc[1]: abort flag, misc[2]: a
+  // softmax warp timed out (read by all four at an item's epilogue barrier)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   namespace tr = trace;
-  const int trace_role = warp == kLoadWarp ? tr::kRoleProducer
-                         : warp == kMmaWarp ? tr::kRoleMma
-                                            : tr::softmax_role(warp);
+  const int trace_role = warp == C::kLoadWarp ? tr::kRoleProducer
+                         : warp == C::kMmaWarp ? tr::kRoleMma
+                                               : tr::softmax_role(warp);
   tr::Recorder rec(p.trace, p.trace_ctas, trace_role, lane == 0);
-  if (warp == kLoadWarp) rec(tr::kCtaStart, tr::sm_id());
+  if (warp == C::kLoadWarp) rec(tr::kCtaStart, tr::sm_id());
 
   const int n_items = num_qblocks * p.H * p.B;
   const unsigned long long limit = p.wait_limit_ns;
   const unsigned long long drain_limit = limit + kDrainExtraNs;
 
   if (threadIdx.x == 0) {
-#pragma unroll
-    for (int t = 0; t < kMaxQTiles; ++t) {
-      ptx::mbar_init(bar_q_full + 8 * t, 1);
-      ptx::mbar_init(bar_s_full + 8 * t, 1);
-      ptx::mbar_init(bar_p_full + 8 * t, 4);  // one arrival per softmax warp
-      ptx::mbar_init(bar_o_full + 8 * t, 1);
-      ptx::mbar_init(bar_q_free + 8 * t, 1);
+    for (int b = 0; b < C::kQBufs; ++b) {
+      ptx::mbar_init(bar_q_full + 8 * b, 1);
+      ptx::mbar_init(bar_q_free + 8 * b, 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(bar_kv_full + 8 * s, 1);
       ptx::mbar_init(bar_kv_empty + 8 * s, 1);
     }
+    ptx::mbar_init(bar_s_full, 1);
+    ptx::mbar_init(bar_s_free, 4);  // one arrival per softmax warp
+    ptx::mbar_init(bar_p_full, 4);
+    ptx::mbar_init(bar_pv_done, 1);
+    ptx::mbar_init(bar_o_full, 1);
+    ptx::mbar_init(bar_o_free, 4);
     ptx::mbar_init(bar_drain, 1);
     misc[1] = 0;
-    misc[2] = misc[3] = 0;  // per tile: a softmax warp timed out
+    misc[2] = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == kLoadWarp && lane == 0) {
+  if (warp == C::kLoadWarp && lane == 0) {
     ptx::tma_prefetch_desc(&tm_q);
     ptx::tma_prefetch_desc(&tm_k);
     ptx::tma_prefetch_desc(&tm_v);
     ptx::tma_prefetch_desc(&tm_o);
   }
-  if (warp == kMmaWarp) {
-    ptx::tmem_alloc(base + C::kMiscOff, kTmemCols);
+  if (warp == C::kMmaWarp) {
+    ptx::tmem_alloc(base + C::kMiscOff, C::kTmemCols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -694,39 +751,35 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
   };
   auto aborted = [&]() { return misc[1] != 0; };
 
-  if (warp == kLoadWarp) {
+  if (warp == C::kLoadWarp) {
     // ===================================================== TMA producer
     if (lane == 0) {
       const uint64_t pol_q = ptx::policy_evict_first();
       const uint64_t pol_kv = ptx::policy_evict_last();
       uint32_t armed = 0, armed_parity = 0;  // per slot: bit set once loaded / last parity
-      int idx = 0;                           // ring entries so far
-      int nq[kMaxQTiles] = {0, 0};           // Q loads per tile so far
+      int idx = 0;                           // ring entries so far: K(n) at 2n, V(n) at 2n + 1
+      int nq = 0;                            // Q loads so far (item u into buffer u & 1)
       bool ok = true;
       for (int k = 0, item; ok && (item = qitem_at(k, n_items)) >= 0; ++k) {
-        const QItem w = decode_qitem<QT>(p, item, num_qblocks);
-#pragma unroll
-        for (int t = 0; t < QT; ++t) {
-          if (!ok || w.lo[t] >= w.hi[t]) continue;
-          // The previous item's O of this tile was staged over its Q
-          // buffer: load the next Q once that store has read it.
-          if (nq[t] > 0 &&
-              (aborted() || !ptx::mbar_wait(bar_q_free + 8 * t,
-                                            static_cast<uint32_t>(nq[t] - 1) & 1u, limit))) {
-            fail();
-            ok = false;
-            break;
-          }
-          ptx::mbar_arrive_expect_tx(bar_q_full + 8 * t, C::kTileBytes);
-#pragma unroll
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            ptx::tma_load_4d(sQ + t * C::kTileBytes + bx * C::kBoxBytes, &tm_q, bar_q_full + 8 * t,
-                             bx * C::kBoxCols, w.h, w.q0[t], w.b, pol_q);
-          ++nq[t];
-          rec(tr::kQLoadIssued, t);
+        const QItem w = decode_qitem(p, item, num_qblocks);
+        if (w.lo >= w.hi) continue;
+        // Buffer qb last held item nq - 2, whose O was staged over it.
+        const int qb = nq & 1;
+        if (nq >= C::kQBufs &&
+            (aborted() || !ptx::mbar_wait(bar_q_free + 8 * qb,
+                                          static_cast<uint32_t>((nq >> 1) - 1) & 1u, limit))) {
+          fail();
+          ok = false;
+          break;
         }
-        // Ring order: K_jlo, V_jlo, K_jlo+1, V_jlo+1, ...
-        for (int j = w.jlo; j < w.jhi && ok; ++j) {
+        ptx::mbar_arrive_expect_tx(bar_q_full + 8 * qb, C::kTileBytes);
+#pragma unroll
+        for (int bx = 0; bx < C::kBoxes; ++bx)
+          ptx::tma_load_4d(sQ + qb * C::kTileBytes + bx * C::kBoxBytes, &tm_q, bar_q_full + 8 * qb,
+                           bx * C::kBoxCols, w.h, w.q0, w.b, pol_q);
+        ++nq;
+        rec(tr::kQLoadIssued, qb);
+        for (int j = w.lo; j < w.hi && ok; ++j) {
           for (int kind = 0; kind < 2; ++kind, ++idx) {
             const int s = idx % C::kStages;
             const uint32_t ph = static_cast<uint32_t>(idx / C::kStages) & 1u;
@@ -750,14 +803,15 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
         }
       }
       // Never leave while a copy of ours may still be writing shared memory.
-#pragma unroll
-      for (int t = 0; t < QT; ++t)
-        if (nq[t] > 0)
-          ptx::mbar_wait(bar_q_full + 8 * t, static_cast<uint32_t>(nq[t] - 1) & 1u, drain_limit);
+      for (int qb = 0; qb < C::kQBufs; ++qb) {
+        const int uses = (nq + C::kQBufs - 1 - qb) / C::kQBufs;
+        if (uses > 0)
+          ptx::mbar_wait(bar_q_full + 8 * qb, static_cast<uint32_t>(uses - 1) & 1u, drain_limit);
+      }
       for (int s = 0; s < C::kStages; ++s)
         if ((armed >> s) & 1u) ptx::mbar_wait(bar_kv_full + 8 * s, (armed_parity >> s) & 1u, drain_limit);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::kMmaWarp) {
     // ===================================================== MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBM, kBN, false, false);
@@ -769,132 +823,86 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
         fail();
         ok = false;
       }
-      // The current item's KV ranges (updated per item; the lambdas read them).
-      int lo[kMaxQTiles] = {0, 0}, hi[kMaxQTiles] = {0, 0};
-      auto in_tile = [&](int t, int j) { return j >= lo[t] && j < hi[t]; };
+      auto wait_bar = [&](uint32_t bar, uint32_t parity) -> bool {
+        if (aborted() || !ptx::mbar_wait(bar, parity, limit)) {
+          fail();
+          return false;
+        }
+        ptx::tc_fence_after();
+        return true;
+      };
       // Wait for ring entry idx; returns its slot or -1 on time-out.
       auto wait_kv = [&](int idx) -> int {
         const int s = idx % C::kStages;
-        const uint32_t ph = static_cast<uint32_t>(idx / C::kStages) & 1u;
-        if (aborted() || !ptx::mbar_wait(bar_kv_full + 8 * s, ph, limit)) {
-          fail();
-          return -1;
-        }
-        ptx::tc_fence_after();
-        return s;
+        return wait_bar(bar_kv_full + 8 * s, static_cast<uint32_t>(idx / C::kStages) & 1u) ? s : -1;
       };
       // K-major Q and K: 8-row groups 8 box rows apart. MN-major V: atoms
       // of kBoxCols columns one box apart.
       const uint64_t dq0 = ptx::smem_desc(sQ, 16, 8 * C::kRowBytes, C::kSwizzle);
       const uint64_t dk0 = ptx::smem_desc(sKV, 16, 8 * C::kRowBytes, C::kSwizzle);
       const uint64_t dv0 = ptx::smem_desc(sKV, C::kBoxBytes, 8 * C::kRowBytes, C::kSwizzle);
-      auto issue_s = [&](int t, int kslot, int j) {
-        const uint64_t dq = dq0 + static_cast<uint32_t>((t * C::kTileBytes) >> 4);
-        const uint64_t dk = dk0 + static_cast<uint32_t>((kslot * C::kTileBytes) >> 4);
+
+      // cs walks the steps whose S is issued, one ahead of cp, whose PV is.
+      StepCursor cs, cp;
+      cs.next_item(p, n_items, num_qblocks);
+      cp = cs;
+      int ns = 0;  // S MMAs issued (global step count)
+      // S(ns) = Q K(j)^T into S's columns; an item's first S waits for its Q.
+      auto issue_s = [&]() -> bool {
+        const int qb = cs.u & 1;
+        if (cs.first()) {
+          if (!wait_bar(bar_q_full + 8 * qb, static_cast<uint32_t>(cs.u >> 1) & 1u)) return false;
+          rec(tr::kQReady, 0);
+        }
+        const int ks = wait_kv(2 * ns);
+        if (ks < 0) return false;
+        const uint64_t dq = dq0 + static_cast<uint32_t>((qb * C::kTileBytes) >> 4);
+        const uint64_t dk = dk0 + static_cast<uint32_t>((ks * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>(
               ((kk / C::kKPerBox) * C::kBoxBytes + (kk % C::kKPerBox) * 32) >> 4);
-          ptx::mma_ss(tmem + t * kBN, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
+          ptx::mma_ss(tmem + C::kColS, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
         }
-        ptx::tc_commit(bar_s_full + 8 * t);
-        rec(tr::kSIssued, (t << 16) | j);
-      };
-      auto issue_pv = [&](int t, int vslot, bool accumulate, int j) {
-        const uint64_t dv = dv0 + static_cast<uint32_t>((vslot * C::kTileBytes) >> 4);
-        const uint32_t acc = accumulate ? 1u : 0u;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          ptx::mma_ts(tmem + C::kColO + t * D, tmem + t * kBN + kk * 8,
-                      dv + static_cast<uint32_t>(kk * (16 * C::kRowBytes >> 4)), kIdescPV,
-                      kk > 0 ? 1u : acc);
-        rec(tr::kPvIssued, (t << 16) | j);
-      };
-      uint32_t p_phase[kMaxQTiles] = {0u, 0u};
-      auto wait_p = [&](int t, int j) -> bool {
-        if (aborted() || !ptx::mbar_wait(bar_p_full + 8 * t, p_phase[t], limit)) {
-          fail();
-          return false;
-        }
-        p_phase[t] ^= 1u;
-        ptx::tc_fence_after();
-        rec(tr::kPSeen, (t << 16) | j);
+        ptx::tc_commit(bar_s_full);
+        ptx::tc_commit(bar_kv_empty + 8 * ks);
+        rec(tr::kSIssued, cs.j);
+        ++ns;
+        cs.advance(p, n_items, num_qblocks);
         return true;
       };
-
-      int base_idx = 0;             // ring entries of the items before this one
-      int nq[kMaxQTiles] = {0, 0};  // Q loads per tile seen so far
-      for (int k = 0, item; ok && (item = qitem_at(k, n_items)) >= 0; ++k) {
-        const QItem w = decode_qitem<QT>(p, item, num_qblocks);
+      if (ok && cs.valid) ok = issue_s();
+      for (int n = 0; ok && cp.valid; ++n) {
+        // The next S, over S(n), as soon as the softmax has read S(n).
+        if (cs.valid && !(wait_bar(bar_s_free, static_cast<uint32_t>(n) & 1u) && issue_s())) {
+          ok = false;
+          break;
+        }
+        // PV(n) once P(n) is stored; an item's first PV (which starts O
+        // afresh) also waits until the previous item's O has been read out.
+        if (!wait_bar(bar_p_full, static_cast<uint32_t>(n) & 1u)) {
+          ok = false;
+          break;
+        }
+        rec(tr::kPSeen, cp.j);
+        const int vs = wait_kv(2 * n + 1);
+        if (vs < 0 || (cp.first() && cp.u > 0 &&
+                       !wait_bar(bar_o_free, static_cast<uint32_t>(cp.u - 1) & 1u))) {
+          ok = false;
+          break;
+        }
+        const uint64_t dv = dv0 + static_cast<uint32_t>((vs * C::kTileBytes) >> 4);
+        const uint32_t acc = cp.first() ? 0u : 1u;
 #pragma unroll
-        for (int t = 0; t < kMaxQTiles; ++t) {
-          lo[t] = w.lo[t];
-          hi[t] = w.hi[t];
-        }
-        const int jlo = w.jlo, jhi = w.jhi;
-#pragma unroll
-        for (int t = 0; t < QT; ++t) {
-          if (ok && lo[t] < hi[t]) {
-            if (!ptx::mbar_wait(bar_q_full + 8 * t, static_cast<uint32_t>(nq[t]) & 1u, limit)) {
-              fail();
-              ok = false;
-            }
-            ++nq[t];
-          }
-        }
-        if (!ok) break;
-        rec(tr::kQReady, 0);
-        {
-          const int ks = wait_kv(base_idx);
-          if (ks < 0) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int t = 0; t < QT; ++t)
-            if (in_tile(t, jlo)) issue_s(t, ks, jlo);
-          ptx::tc_commit(bar_kv_empty + 8 * ks);
-        }
-        for (int j = jlo; ok && j < jhi; ++j) {
-          const int rel = j - jlo;
-          const int vs = wait_kv(base_idx + 2 * rel + 1);
-          if (vs < 0) {
-            ok = false;
-            break;
-          }
-          if (in_tile(0, j)) {
-            if (!wait_p(0, j)) {
-              ok = false;
-              break;
-            }
-            issue_pv(0, vs, j > lo[0], j);
-            if (j == hi[0] - 1) ptx::tc_commit(bar_o_full);
-          }
-          const bool has_next = j + 1 < jhi;
-          int ks = -1;
-          if (has_next) {
-            ks = wait_kv(base_idx + 2 * rel + 2);
-            if (ks < 0) {
-              ok = false;
-              break;
-            }
-            if (in_tile(0, j + 1)) issue_s(0, ks, j + 1);
-          }
-          if (QT > 1 && in_tile(1, j)) {
-            if (!wait_p(1, j)) {
-              ok = false;
-              break;
-            }
-            issue_pv(1, vs, j > lo[1], j);
-            if (j == hi[1] - 1) ptx::tc_commit(bar_o_full + 8);
-          }
-          ptx::tc_commit(bar_kv_empty + 8 * vs);
-          if (has_next) {
-            if (QT > 1 && in_tile(1, j + 1)) issue_s(1, ks, j + 1);
-            ptx::tc_commit(bar_kv_empty + 8 * ks);
-          }
-        }
-        base_idx += 2 * (jhi - jlo);
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          ptx::mma_ts(tmem + C::kColO, tmem + C::kColP + kk * 8,
+                      dv + static_cast<uint32_t>(kk * (16 * C::kRowBytes >> 4)), kIdescPV,
+                      kk > 0 ? 1u : acc);
+        ptx::tc_commit(bar_pv_done);
+        ptx::tc_commit(bar_kv_empty + 8 * vs);
+        if (cp.last()) ptx::tc_commit(bar_o_full);
+        rec(tr::kPvIssued, cp.j);
+        cp.advance(p, n_items, num_qblocks);
       }
       // Every MMA must have finished before tensor memory is released.
       ptx::tc_commit(bar_drain);
@@ -903,42 +911,40 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
     }
     __syncwarp();
   } else {
-    // ===================================================== softmax warpgroups
-    const int t = warp >> 2;
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_base + t * kBN;
-    const uint32_t tO = tmem + lane_base + C::kColO + t * D;
+    // ===================================================== softmax warpgroup
+    const int row = warp * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_base + C::kColS;
+    const uint32_t tO = tmem + lane_base + C::kColO;
+    const uint32_t tP = tmem + lane_base + C::kColP;
     const float c = p.scale_log2;
     // A zero scale makes every visible score 0: use 0 as the score and 1 as
     // the multiplier.
     const bool zero_scale = !(c > 0.f);
     const float ce = zero_scale ? 1.f : c;
+    // Bounded wait of all 32 lanes; a time-out is recorded once.
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      bool wv = ptx::mbar_wait(bar, parity, limit);
+      wv = __all_sync(0xffffffffu, wv);
+      if (!wv) fail();
+      return wv;
+    };
 
     bool ok = true;
-    uint32_t s_phase = 0;  // parity of the S(t) MMAs seen so far
-    int nw = 0;            // items with work for this tile so far
+    int n = 0;  // KV steps so far (global, across items)
+    int u = 0;  // items with work so far
     for (int k = 0; ok; ++k) {
       const int item = qitem_at(k, n_items);
       if (item < 0) break;
-      const QItem w = decode_qitem<QT>(p, item, num_qblocks);
-      // This warpgroup's tile, selected without run-time array indexing.
-      const int tq0 = t == 0 ? w.q0[0] : w.q0[1];
-      const int tlo = t == 0 ? w.lo[0] : w.lo[1];
-      const int thi = t == 0 ? w.hi[0] : w.hi[1];
-      if (tlo >= thi) continue;
-      const int i = tq0 + row;
+      const QItem w = decode_qitem(p, item, num_qblocks);
+      if (w.lo >= w.hi) continue;
+      const int i = w.q0 + row;
       const RowBounds rb = row_bounds(p, i);
 
       float m_use = -INFINITY;  // running max of score * scale * log2(e) (possibly stale)
       float l_run = 0.f;        // running sum of 2^(x - m_use)
-      for (int j = tlo; j < thi; ++j) {
-        bool wv = ptx::mbar_wait(bar_s_full + 8 * t, s_phase, limit);
-        s_phase ^= 1u;
-        wv = __all_sync(0xffffffffu, wv);
-        if (!wv) {
-          fail();
+      for (int j = w.lo; j < w.hi; ++j, ++n) {
+        if (!wait_all(bar_s_full, static_cast<uint32_t>(n) & 1u)) {
           ok = false;
           break;
         }
@@ -950,13 +956,17 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
         for (int c0 = 0; c0 < kBN; c0 += 32) ptx::tmem_ld_32x32b_x32(tS + c0, r + c0);
         ptx::tmem_wait_ld();
         ptx::reg_fence<kBN>(r);
+        // S(n) is in registers: the next S may be computed over it.
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_s_free);
         rec(tr::kSLoaded, j);
 
         const int k0 = j * kBN;
         bool full = k0 + kBN <= p.S;
-        if (p.causal) full = full && (k0 + kBN - 1 <= tq0);
-        if (p.window > 0) full = full && (tq0 + kBM - 1 - k0 < p.window);
-        if (p.window > 0 && !p.causal) full = full && (k0 + kBN - 1 - tq0 < p.window);
+        if (p.causal) full = full && (k0 + kBN - 1 <= w.q0);
+        if (p.window > 0) full = full && (w.q0 + kBM - 1 - k0 < p.window);
+        if (p.window > 0 && !p.causal) full = full && (k0 + kBN - 1 - w.q0 < p.window);
         const int vlo = rb.lo == INT_MIN ? INT_MIN : rb.lo - k0;
         const int vhi = rb.hi - k0;
 
@@ -972,7 +982,7 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
         }
         const float m_tile = mx == -INFINITY ? -INFINITY : mx * ce;
         const float m_new = fmaxf(m_use, m_tile);
-        const bool first = j == tlo;
+        const bool first = j == w.lo;
         float alpha = 1.f;
         bool rescale = false;
         if (first) {
@@ -984,19 +994,27 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
         }
         const float neg_base = m_use == -INFINITY ? 0.f : -m_use;
 
-        // P = 2^(x - m_use) (hidden scores are -inf and give 0) as bf16 pairs
-        // written over S, and the row sum.
+        // P = 2^(x - m_use) (hidden scores are -inf and give 0) as bf16
+        // pairs, and the row sum.
         const float row_sum = tile::exp2_to_bf16(r, ce, neg_base);
         l_run = l_run * alpha + row_sum;
         if (FA_TRACE) {
           asm volatile("" ::"f"(l_run), "r"(r[0]), "r"(r[63]));
           rec(tr::kExpDone, j);
         }
+        // PV(n - 1) reads P's columns and accumulates into O: it must have
+        // completed before P is overwritten or O corrected.
+        if (n > 0) {
+          if (!wait_all(bar_pv_done, static_cast<uint32_t>(n - 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+        }
 #pragma unroll
-        for (int c0 = 0; c0 < kBN / 2; c0 += 32) ptx::tmem_st_32x32b_x32(tS + c0, r + c0);
+        for (int c0 = 0; c0 < kBN / 2; c0 += 32) ptx::tmem_st_32x32b_x32(tP + c0, r + c0);
 
-        // Lazy correction of the O accumulator (previous PV has completed:
-        // the S MMA this iteration waited for was issued after it).
+        // Lazy correction of the O accumulator.
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -1012,56 +1030,51 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_p_full + 8 * t);
+        if (lane == 0) ptx::mbar_arrive(bar_p_full);
         rec(tr::kPReady, j | (rescale ? 1u << 23 : 0u));
       }
 
-      // ---- epilogue: O / l -> bf16 -> shared (swizzled, over this tile's Q
-      // buffer: its S MMAs are done) -> TMA store; LSE. A warp that timed out
-      // records it in misc[2 + t] before the tile's barrier, so the four warps
-      // leave together.
-      if (ok) {
-        bool wv = ptx::mbar_wait(bar_o_full + 8 * t, static_cast<uint32_t>(nw) & 1u, limit);
-        wv = __all_sync(0xffffffffu, wv);
-        if (!wv) {
-          fail();
-          ok = false;
-        }
-      }
-      if (!ok && lane == 0) misc[2 + t] = 1;
+      // ---- epilogue: O -> registers (then O's columns go back to the MMA
+      // thread) -> O / l as bf16 in shared memory, swizzled, over this item's
+      // Q buffer (its S MMAs are done) -> TMA store; LSE. A warp that timed
+      // out records it in misc[2] before the barrier, so the four warps leave
+      // together.
+      if (ok && !wait_all(bar_o_full, static_cast<uint32_t>(u) & 1u)) ok = false;
+      if (!ok && lane == 0) misc[2] = 1;
       // A store of rows that start past S would be a planning error.
-      const bool do_store = ok && tr::guard(tq0 < p.S, p.status, kStatusBoundsGuard);
+      const bool do_store = ok && tr::guard(w.q0 < p.S, p.status, kStatusBoundsGuard);
+      const int qb = u & 1;
       if (do_store) {
         rec(tr::kEpilogueStart, 0);
         ptx::tc_fence_after();
         const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-        uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
+        uint8_t* stage = smem + C::kQOff + qb * C::kTileBytes;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
           ptx::tmem_ld_32x32b_x32(tO + c0, o);
           ptx::tmem_wait_ld();
           ptx::reg_fence<32>(o);
-          if (D == 96)
-            tile::stage_bf16_sw64(stage, C::kBoxBytes, row, c0, o, inv_l);
-          else
-            tile::stage_bf16_sw128(stage, C::kBoxBytes, row, c0, o, inv_l);
+          tile::stage_bf16_sw128(stage, C::kBoxBytes, row, c0, o, inv_l);
         }
-        ptx::fence_proxy_async_smem();
       }
-      ptx::named_bar_sync(1 + t, 128);
-      const bool failed = misc[2 + t] != 0;
-      if (quad == 0 && lane == 0) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_o_free);
+      if (do_store) ptx::fence_proxy_async_smem();
+      ptx::named_bar_sync(1, 128);
+      const bool failed = misc[2] != 0;
+      if (warp == 0 && lane == 0) {
         if (!failed && do_store) {
 #pragma unroll
           for (int bx = 0; bx < C::kBoxes; ++bx)
-            ptx::tma_store_4d(&tm_o, sQ + t * C::kTileBytes + bx * C::kBoxBytes,
-                              bx * C::kBoxCols, w.h, tq0, w.b);
+            ptx::tma_store_4d(&tm_o, sQ + qb * C::kTileBytes + bx * C::kBoxBytes, bx * C::kBoxCols,
+                              w.h, w.q0, w.b);
           ptx::tma_store_commit();
           ptx::tma_store_wait_read();
         }
-        // This tile's Q buffer may take the next item's Q.
-        ptx::mbar_arrive(bar_q_free + 8 * t);
+        // This Q buffer may take the item after next's Q.
+        ptx::mbar_arrive(bar_q_free + 8 * qb);
       }
       if (failed) {
         ok = false;
@@ -1076,15 +1089,15 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
           p.lse[idx] = (m_fin + __log2f(l_run)) * kLn2;
       }
       if (do_store) rec(tr::kEpilogueEnd, 0);
-      ++nw;
+      ++u;
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -1107,17 +1120,18 @@ cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* 
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
   // One-tile CTAs, more items than resident slots: the persistent kernel
   // (not in the debug build, whose trace records one item per CTA).
-  if constexpr (QT == 1 && !FA_TRACE) {
-    const long long slots = static_cast<long long>(p.num_sms) * Roles<QT>::kCtasPerSm;
+  if constexpr (QT == 1 && D == 64 && !FA_TRACE) {
+    using PC = PCfg<D>;
+    const long long slots = static_cast<long long>(p.num_sms) * PC::kCtasPerSm;
     if (p.num_sms > 0 && grid > slots) {
       static unsigned long long attr_done = 0;
-      cudaError_t err = ensure_smem_attr(&attr_done, reinterpret_cast<const void*>(
-                                                         &fa_fwd_bf16_tc_persistent_kernel<D, QT>),
-                                         C::kSmemBytes);
+      cudaError_t err = ensure_smem_attr(
+          &attr_done, reinterpret_cast<const void*>(&fa_fwd_bf16_tc_persistent_kernel<D>),
+          PC::kSmemBytes);
       if (err != cudaSuccess) return err;
-      fa_fwd_bf16_tc_persistent_kernel<D, QT>
-          <<<static_cast<unsigned>(slots), Roles<QT>::kThreads, C::kSmemBytes, stream>>>(
-              tq, tk, tv, to, p, nqb);
+      fa_fwd_bf16_tc_persistent_kernel<D>
+          <<<static_cast<unsigned>(slots), PC::kThreads, PC::kSmemBytes, stream>>>(tq, tk, tv, to,
+                                                                                    p, nqb);
       return cudaGetLastError();
     }
   }

@@ -45,6 +45,36 @@ def test_bounded_wait_timeout_is_reported_and_recoverable(oracle_mod):
     assert fa.device_status() == fa.FA_OK
 
 
+def test_bounded_wait_timeout_on_the_persistent_schedule(oracle_mod):
+    """The same stall probe on the persistent one-tile kernel (head dim 64,
+    S 1024, more query tiles than resident CTAs): the MMA thread gives up,
+    the softmax warps' waits expire and they leave their item loop together,
+    the producer drains its copies; the next call is correct."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    fa.build()
+    dev = torch.device("cuda:0")
+    q, k, v = make_qkv(4, 1024, 16, 16, 64, torch.bfloat16, seed=23)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    scale = 1.0 / math.sqrt(64)
+    assert fa.device_status(clear=True) == fa.FA_OK
+    old = fa.set_wait_timeout_ns(20_000_000)
+    fa.set_stall_probe(True)
+    try:
+        fa.mha_no_cache(qd, kd, vd, scale, "causal")
+        assert fa.device_status(clear=True) == fa.FA_ERR_TIMEOUT
+    finally:
+        fa.set_stall_probe(False)
+        fa.set_wait_timeout_ns(old)
+    assert fa.device_status(clear=True) == fa.FA_OK
+    out = fa.mha_no_cache(qd, kd, vd, scale, "causal")
+    torch.cuda.synchronize()
+    ref, _ = oracle_mod.mha_forward(q, k, v, scale, True, -1)
+    err = (out.double().cpu() - torch.from_numpy(ref)).abs()
+    assert err.max().item() <= 2e-2 and err.mean().item() <= 2e-3
+    assert fa.device_status() == fa.FA_OK
+
+
 def test_timeout_is_reported_on_its_own_stream_only(oracle_mod):
     """fa_stream_status reads the status word of one stream, ordered on that
     stream: a time-out on stream A shows on A and not on B, and reading it
