@@ -16,7 +16,8 @@
 //   * S = Q K^T and O += P V are tcgen05.mma (bf16 in, fp32 accumulate) with
 //     S, P and O resident in tensor memory: S_t at columns [128t, 128t+128),
 //     P_t (bf16 pairs) written over the first 64 of them, O_t at
-//     [256 + D t, 256 + D (t+1));
+//     [256 + D t, 256 + D (t+1)); one-tile CTAs run a persistent kernel that
+//     gives P its own columns and computes S(j+1) during the softmax of j;
 //   * warp roles: warps 0-3 and 4-7 are the softmax warpgroups of Q tile 0 and
 //     1 (thread = query row = TMEM lane), then one warp issues the MMAs and
 //     one the TMA loads. The MMA order S0 S1 | PV0 S0' PV1 S1' | ... lets one
@@ -41,6 +42,7 @@
 // fa_trace.cuh; in the default build both compile to nothing.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 
@@ -562,9 +564,9 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
 // item, and the first S of an item is computed during the previous item's
 // epilogue; the epilogue hands O back to the MMA thread (o_free) as soon as
 // it has read it out of tensor memory. The ring, the phases and the counts
-// carry on from one item to the next. Used for one-tile CTAs when the items
-// outnumber the resident slots (short sequences, whose items are a few KV
-// steps each).
+// carry on from one item to the next. Used for every one-tile launch (short
+// sequences, whose items are a few KV steps each); with fewer items than
+// resident slots each CTA takes one item and still gains the early S.
 //
 // TMEM columns: S [0, 128), O [128, 128 + D), P [128 + D, 128 + D + 64).
 template <int D>
@@ -1118,20 +1120,21 @@ cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* 
   const int nqb = (p.S + QT * kBM - 1) / (QT * kBM);
   const long long grid = static_cast<long long>(nqb) * p.H * p.B;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  // One-tile CTAs, more items than resident slots: the persistent kernel
-  // (not in the debug build, whose trace records one item per CTA).
+  // One-tile CTAs: the persistent kernel, with as many CTAs as there are
+  // items or resident slots (not in the debug build, whose trace records one
+  // item per CTA).
   if constexpr (QT == 1 && D == 64 && !FA_TRACE) {
     using PC = PCfg<D>;
-    const long long slots = static_cast<long long>(p.num_sms) * PC::kCtasPerSm;
-    if (p.num_sms > 0 && grid > slots) {
+    const long long ctas = std::min(grid, static_cast<long long>(p.num_sms) * PC::kCtasPerSm);
+    if (p.num_sms > 0) {
       static unsigned long long attr_done = 0;
       cudaError_t err = ensure_smem_attr(
           &attr_done, reinterpret_cast<const void*>(&fa_fwd_bf16_tc_persistent_kernel<D>),
           PC::kSmemBytes);
       if (err != cudaSuccess) return err;
       fa_fwd_bf16_tc_persistent_kernel<D>
-          <<<static_cast<unsigned>(slots), PC::kThreads, PC::kSmemBytes, stream>>>(tq, tk, tv, to,
-                                                                                    p, nqb);
+          <<<static_cast<unsigned>(ctas), PC::kThreads, PC::kSmemBytes, stream>>>(tq, tk, tv, to,
+                                                                                   p, nqb);
       return cudaGetLastError();
     }
   }

@@ -138,6 +138,8 @@ extern "C" fa_status_t fa_mha_no_cache_noalloc(void* out, float* lse, const void
   p.wait_limit_ns = fa::wait_limit_ns();  // the limit fa_set_wait_timeout_ns sets
   p.stall_probe = 0;
   p.cache_maps = false;  // the tensor-map cache grows a host hash table
+  // SM count for the persistent schedules (a device attribute: no allocation)
+  cudaDeviceGetAttribute(&p.num_sms, cudaDevAttrMultiProcessorCount, dev);
   err = fa::launch_fwd_bf16_tc(p, out, q, k, v, s);
   if (err != cudaSuccess)
     return noalloc_fail(FA_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(err));
