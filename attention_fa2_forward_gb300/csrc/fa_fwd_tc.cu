@@ -423,10 +423,12 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
       rec(tr::kSReady, j);
 
       uint32_t r[kBN];
+      float pm[kBN / 32];  // maximum of each 32 columns, reduced by the load
 #pragma unroll
-      for (int c0 = 0; c0 < kBN; c0 += 32) ptx::tmem_ld_32x32b_x32(tS + c0, r + c0);
+      for (int c0 = 0; c0 < kBN; c0 += 32) ptx::tmem_ld_max_32x32b_x32(tS + c0, r + c0, &pm[c0 / 32]);
       ptx::tmem_wait_ld();
       ptx::reg_fence<kBN>(r);
+      tile::float_fence<kBN / 32>(pm);
       rec(tr::kSLoaded, j);
 
       const int k0 = j * kBN;
@@ -441,8 +443,13 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
       // invisible scores in place, then every tile takes the same path.
       if (!full || zero_scale) tile::mask_cols(r, vlo, vhi, zero_scale);
 
-      // Row maximum of the (visible) scores.
-      const float mx = tile::row_max(r);
+      // Row maximum of the (visible) scores: from the loads' reductions when
+      // every score is visible, else over the masked registers.
+      float mx;
+      if (full && !zero_scale)
+        mx = tile::max_of(pm);
+      else
+        mx = tile::row_max(r);
       if (FA_TRACE) {
         asm volatile("" ::"f"(mx));
         rec(tr::kMaxDone, j);
@@ -954,10 +961,13 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, PCfg<D>::kCtasPerSm)
         rec(tr::kSReady, j);
 
         uint32_t r[kBN];
+        float pm[kBN / 32];  // maximum of each 32 columns, reduced by the load
 #pragma unroll
-        for (int c0 = 0; c0 < kBN; c0 += 32) ptx::tmem_ld_32x32b_x32(tS + c0, r + c0);
+        for (int c0 = 0; c0 < kBN; c0 += 32)
+          ptx::tmem_ld_max_32x32b_x32(tS + c0, r + c0, &pm[c0 / 32]);
         ptx::tmem_wait_ld();
         ptx::reg_fence<kBN>(r);
+        tile::float_fence<kBN / 32>(pm);
         // S(n) is in registers: the next S may be computed over it.
         ptx::tc_fence_before();
         __syncwarp();
@@ -976,8 +986,13 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, PCfg<D>::kCtasPerSm)
         // invisible scores in place, then every tile takes the same path.
         if (!full || zero_scale) tile::mask_cols(r, vlo, vhi, zero_scale);
 
-        // Row maximum of the (visible) scores.
-        const float mx = tile::row_max(r);
+        // Row maximum of the (visible) scores: from the loads' reductions
+        // when every score is visible, else over the masked registers.
+        float mx;
+        if (full && !zero_scale)
+          mx = tile::max_of(pm);
+        else
+          mx = tile::row_max(r);
         if (FA_TRACE) {
           asm volatile("" ::"f"(mx));
           rec(tr::kMaxDone, j);

@@ -50,6 +50,19 @@ __device__ __forceinline__ float row_max(const uint32_t* r) {
   return ptx::max3(a0, a1, fmaxf(a2, a3));
 }
 
+// After tmem_wait_ld(), pass each reduced maximum through an empty asm so
+// that no use of it can be scheduled above the wait.
+template <int N>
+__device__ __forceinline__ void float_fence(float* m) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+f"(m[i]));
+}
+
+// Maximum of the four per-32-column maxima of a 128-column tile.
+__device__ __forceinline__ float max_of(const float* pm) {
+  return ptx::max3(pm[0], pm[1], fmaxf(pm[2], pm[3]));
+}
+
 // P = 2^(s * ce + neg_base) for the N held scores (hidden scores are -inf
 // and give 0), written as N/2 bf16 pairs over r[0..N/2-1]; returns the fp32
 // sum of the (unrounded) P. Pairs of columns use packed FMAs and adds.
