@@ -642,10 +642,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
 
         uint32_t s[kBN];
+        float pm[kBN / 32];  // maximum of each 32 columns, reduced by the load
 #pragma unroll
-        for (int c0 = 0; c0 < kBN; c0 += 32) ptx::tmem_ld_32x32b_x32(tS + c0, s + c0);
+        for (int c0 = 0; c0 < kBN; c0 += 32) ptx::tmem_ld_max_32x32b_x32(tS + c0, s + c0, &pm[c0 / 32]);
         ptx::tmem_wait_ld();
         ptx::reg_fence<kBN>(s);
+        tile::float_fence<kBN / 32>(pm);
 
         // Rows that are not real (padding) are never stored: skip their mask.
         const int k0 = (I.jlo + r) * kBN;
@@ -653,7 +655,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!full || zero_scale)
           tile::mask_cols(s, valid ? vlo - k0 : 0, valid ? vhi - k0 : kBN - 1, zero_scale);
 
-        const float mx = tile::row_max(s);
+        // Row maximum: from the loads' reductions when no score is hidden.
+        float mx;
+        if (full && !zero_scale)
+          mx = tile::max_of(pm);
+        else
+          mx = tile::row_max(s);
         const float m_tile = mx == -INFINITY ? -INFINITY : mx * ce;
         const float m_new = fmaxf(m_use, m_tile);
         float alpha = 1.f;

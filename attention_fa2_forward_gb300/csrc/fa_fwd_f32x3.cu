@@ -403,10 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_after();
       uint32_t s[kBN];
-      ptx::tmem_ld_32x32b_x32(tS, s);
-      ptx::tmem_ld_32x32b_x32(tS + 32, s + 32);
+      float pm[2];  // maximum of each 32 columns, reduced by the load
+      ptx::tmem_ld_max_32x32b_x32(tS, s, &pm[0]);
+      ptx::tmem_ld_max_32x32b_x32(tS + 32, s + 32, &pm[1]);
       ptx::tmem_wait_ld();
       ptx::reg_fence<kBN>(s);
+      asm volatile("" : "+f"(pm[0]), "+f"(pm[1]));  // no use above the wait
 
       const int k0 = (jlo + r) * kBN;
       bool full = k0 + kBN <= p.S;
@@ -416,10 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!full || zero_scale)
         mask_cols64(s, vlo == INT_MIN ? INT_MIN : vlo - k0, vhi - k0, zero_scale);
 
+      // Row maximum: from the loads' reductions when no score is hidden.
       float mx = -INFINITY;
+      if (full && !zero_scale) {
+        mx = fmaxf(pm[0], pm[1]);
+      } else {
 #pragma unroll
-      for (int e = 0; e < kBN; e += 2)
-        mx = ptx::max3(mx, __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+        for (int e = 0; e < kBN; e += 2)
+          mx = ptx::max3(mx, __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+      }
       const float m_tile = mx == -INFINITY ? -INFINITY : mx * ce;
       const float m_new = fmaxf(m_use, m_tile);
       float alpha = 1.f;
