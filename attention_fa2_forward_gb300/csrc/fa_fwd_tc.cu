@@ -9,8 +9,7 @@
 // the end), mapped onto Blackwell hardware:
 //
 //   * one CTA owns two 128-row Q tiles of one (b, h) -- or, for head dims up
-//     to 64 and sequences up to 1024, one Q tile, with two CTAs per SM -- and
-//     streams the K/V tiles
+//     to 64, one Q tile, with two CTAs per SM -- and streams the K/V tiles
 //     they need through a shared-memory ring (TMA, swizzled, straight from
 //     BSHD: the Step 0 / Step 4 transposes are the tensor maps' strides);
 //   * S = Q K^T and O += P V are tcgen05.mma (bf16 in, fp32 accumulate) with
@@ -1163,12 +1162,15 @@ cudaError_t launch_d(const FwdProblem& p, void* out, const void* q, const void* 
   return cudaGetLastError();
 }
 
-// Q tiles per CTA: one for head dims up to 64 and sequences up to 1024 --
-// a CTA of one tile fits twice on an SM, and on short sequences, whose tiles
-// see few KV steps, one CTA's set-up and epilogue then overlap the other's
-// work (B4 H16 S1024 D64 causal: 280 -> 302 TFLOP/s; B8 S512: 174 -> 204) --
-// else two (one-tile CTAs lose ~4 % on S >= 2048).
-int q_tiles_per_cta(int D, int S) { return D <= 64 && S <= 1024 ? 1 : 2; }
+// Q tiles per CTA: one for head dims up to 64 -- a CTA of one tile fits
+// twice on an SM and, run persistent with P in its own tensor-memory
+// columns, computes S(j+1) during the softmax of j (B1 H16 S8192 D64 causal
+// 786 -> 1005 TFLOP/s against two-tile CTAs; B4 H16 S1024: 280 -> 377) --
+// else two (one CTA per SM; no tensor-memory room for P of its own).
+int q_tiles_per_cta(int D, int S) {
+  (void)S;
+  return D <= 64 ? 1 : 2;
+}
 
 }  // namespace
 
@@ -1181,9 +1183,7 @@ cudaError_t launch_fwd_bf16_tc(const FwdProblem& p, void* out, const void* q, co
                                const void* v, cudaStream_t stream) {
   // Head dims up to 64 (96, 128) run on the 64 (96, 128) column kernel.
   if (p.D % 8 != 0 || p.D < 8 || p.D > 128) return cudaErrorInvalidValue;
-  if (p.D <= 64)
-    return q_tiles_per_cta(p.D, p.S) == 1 ? launch_d<64, 1>(p, out, q, k, v, stream)
-                                          : launch_d<64, 2>(p, out, q, k, v, stream);
+  if (p.D <= 64) return launch_d<64, 1>(p, out, q, k, v, stream);
   if (p.D <= 96) return launch_d<96, 2>(p, out, q, k, v, stream);
   return launch_d<128, 2>(p, out, q, k, v, stream);
 }

@@ -155,10 +155,11 @@ def test_trace_and_guard_knobs_are_debug_only(lib):
 
 def test_trace_cta_count_follows_the_prefill_grid(lib):
     # one CTA per (query block, head, batch): blocks of 128 queries (one Q
-    # tile) for head dims up to 64 and S up to 1024, else of 256 (two tiles);
-    # head dims above 128 run another kernel and have no trace
+    # tile) for head dims up to 64, else of 256 (two tiles); head dims above
+    # 128 run another kernel and have no trace
     assert lib.fa_trace_ctas(4, 1024, 16, 64) == 8 * 16 * 4
-    assert lib.fa_trace_ctas(4, 1025, 16, 64) == 5 * 16 * 4
+    assert lib.fa_trace_ctas(4, 1025, 16, 64) == 9 * 16 * 4
+    assert lib.fa_trace_ctas(1, 4096, 2, 40) == 32 * 2
     assert lib.fa_trace_ctas(4, 1024, 16, 72) == 4 * 16 * 4
     assert lib.fa_trace_ctas(2, 4097, 32, 128) == 17 * 32 * 2
     assert lib.fa_trace_ctas(1, 1, 1, 8) == 1

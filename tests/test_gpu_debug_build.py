@@ -64,7 +64,7 @@ def test_trace_matches_the_launch(B, S, H, Hkv, D, causal, window):
     assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
 
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    tiles = 1 if D <= 64 and S <= 1024 else 2  # Q tiles of 128 rows per CTA
+    tiles = 1 if D <= 64 else 2  # Q tiles of 128 rows per CTA
     nqb = (S + 128 * tiles - 1) // (128 * tiles)
     assert len(events) == nqb * H * B
     eff_window = window if 0 < window < S else -1

@@ -104,7 +104,22 @@ def test_persistent_short_sequence_schedule(oracle_mod, B, S, H, Hkv, D, causal,
     _full_case(oracle_mod, B, S, H, Hkv, D, torch.bfloat16, causal, window, seed=900 + S + H)
 
 
-@pytest.mark.parametrize("B,S,H,Hkv,causal", [(4, 1024, 16, 16, True), (6, 640, 16, 4, False)])
+@pytest.mark.parametrize("B,S,H,Hkv,D,causal,window", [
+    (1, 4096, 8, 2, 64, True, -1),     # GQA, 32 KV steps for the last query tiles
+    (1, 2048, 8, 8, 64, False, 700),   # two-sided window, no causal mask
+    (2, 3000, 4, 1, 48, True, -1),     # MQA, padded head dim, ragged last tile
+    (1, 8192, 2, 1, 64, True, 3000),   # causal window over a long sequence
+])
+def test_one_tile_kernel_long_sequences(oracle_mod, B, S, H, Hkv, D, causal, window):
+    """Head dims up to 64 run one Q tile per CTA at every length: long
+    sequences give the persistent kernel items of many KV steps (the ring,
+    the S/P/PV barriers and the lazy rescale over dozens of steps); every
+    element and LSE row is checked."""
+    _full_case(oracle_mod, B, S, H, Hkv, D, torch.bfloat16, causal, window, seed=970 + S + H)
+
+
+@pytest.mark.parametrize("B,S,H,Hkv,causal", [(4, 1024, 16, 16, True), (6, 640, 16, 4, False),
+                                              (1, 4096, 4, 4, True)])
 def test_persistent_short_sequence_large_logits(oracle_mod, B, S, H, Hkv, causal):
     """Large logits (q, k ~ N(0, 3^2): scores with a standard deviation of
     about 9) on the persistent one-tile schedule: the running maximum jumps by
