@@ -372,10 +372,11 @@ fa_status_t fa_trace_set_buffer(void *buf, unsigned long long bytes);
 unsigned long long fa_trace_bytes_per_cta(void);
 
 /*
- * fa_trace_ctas -- CTAs of one bf16 prefill launch (D <= 128) for these
- * sizes: one per (query block, head, batch), blocks of 128 queries for D up
- * to 64 with S up to 1024, else of 256; 0 for sizes that launch another
- * kernel.
+ * fa_trace_ctas -- CTAs of one bf16 prefill launch of the debug build
+ * (D <= 128) for these sizes: one per (query block, head, batch), blocks of
+ * 128 queries for D up to 64, else of 256; 0 for sizes that launch another
+ * kernel. (The default build runs head dims up to 64 on a persistent grid of
+ * at most two CTAs per SM instead.)
  */
 long long fa_trace_ctas(int B, int S, int H, int D);
 
