@@ -570,9 +570,9 @@ __global__ void __launch_bounds__(Roles<QT>::kThreads, Roles<QT>::kCtasPerSm)
 // item, and the first S of an item is computed during the previous item's
 // epilogue; the epilogue hands O back to the MMA thread (o_free) as soon as
 // it has read it out of tensor memory. The ring, the phases and the counts
-// carry on from one item to the next. Used for every one-tile launch (short
-// sequences, whose items are a few KV steps each); with fewer items than
-// resident slots each CTA takes one item and still gains the early S.
+// carry on from one item to the next. Used for every launch with a head dim
+// up to 64, at every length; with fewer items than resident slots each CTA
+// takes one item and still gains the early S.
 //
 // TMEM columns: S [0, 128), O [128, 128 + D), P [128 + D, 128 + D + 64).
 template <int D>
