@@ -328,6 +328,28 @@ def test_packed_qkv_slices_and_strided_output(oracle_mod, dtype, D):
     assert torch.isnan(wide[:, :, 0]).all() and torch.isnan(wide[:, :, 1 + H:]).all()
 
 
+@pytest.mark.parametrize("D", [64, 48])
+def test_packed_qkv_slices_long_sequence_one_tile_kernel(oracle_mod, D):
+    """Head dims up to 64 on the persistent one-tile kernel through strided
+    views: packed [B, S, H + 2 Hkv, D] slices, 320 query tiles (more than the
+    resident CTAs, so CTAs walk several), output into a slice of a wider
+    buffer whose other heads stay untouched."""
+    B, S, H, Hkv = 2, 2500, 8, 4
+    q, k, v = make_qkv(B, S, H, Hkv, D, torch.bfloat16, seed=43 + D)
+    dev = torch.device("cuda:0")
+    qkv = torch.cat([q, k, v], dim=2).to(dev)
+    qs, ks, vs = qkv[:, :, :H], qkv[:, :, H:H + Hkv], qkv[:, :, H + Hkv:]
+    wide = torch.full((B, S, H + 2, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    out = wide[:, :, 2:]
+    scale = 1.0 / math.sqrt(D)
+    _, lse = fa.mha_no_cache(qs, ks, vs, scale, "causal", out=out, return_lse=True)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle_mod.mha_forward(q, k, v, scale, True, -1)
+    _compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+             torch.bfloat16, f"packed qkv D{D} S{S}")
+    assert torch.isnan(wide[:, :, :2]).all()
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 def test_bhsd_tensors_viewed_as_bshd(oracle_mod, dtype):
     """[B, H, S, D] storage read and written through BSHD views."""
